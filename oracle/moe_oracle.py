@@ -1,0 +1,335 @@
+"""CPU oracle for the forward pass of a token-choice top-k MoE SwiGLU layer.
+
+TEST INFRASTRUCTURE ONLY. This module is the slow, plain reference that the
+CUDA library is checked against. Only ``tests/``, ``__graft_entry__.smoke()``
+and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import
+it. The library's product path never calls it, and it shares no code with the
+CUDA sources.
+
+Everything here works in float64 on numpy arrays built from the exact values
+of the (possibly bf16-rounded) inputs. Each function restates one step of the
+method as the pages define it; the citation names the page title and the
+section or formula.
+
+Pages cited
+-----------
+[P1] "MOE 专家选择与路由机制" (wuhy-notes)
+[P2] "MoE：router 怎样选 expert" (cooking-agi, router page)
+[P3] pwwt.cn blog on MoE routing, §2.1 "Top-K取法的工作细节"
+[P4] "拆解 MoE：单个 Token 如何经过专家层"
+[P5] "【大模型】MoE（专家混合模型）简介"
+
+Readings taken where the pages leave a step open (each is listed with its
+reason in the design notes of the repository):
+* ties in top-k go to the lower expert index; selected slots are ordered by
+  descending selection score, then ascending index;
+* the per-expert bias enters the selection score only; gates use the
+  un-biased scores;
+* sigmoid + renormalise divides each selected sigmoid score by the sum over
+  the selected experts, with no further scale;
+* rows of the dispatched layout are ordered by (expert ascending, token
+  ascending);
+* no capacity limit, nothing dropped.
+
+Pinned by ``tests/test_oracle_pins.py`` against the worked examples the pages
+print, closed forms, library routines and brute force. Every function below
+has at least one pin.
+"""
+from __future__ import annotations
+
+import itertools
+
+import numpy as np
+
+SOFTMAX = "softmax"
+SIGMOID = "sigmoid"
+NORM_SELECTED = "selected"
+NORM_NONE = "none"
+
+
+# --------------------------------------------------------------------------
+# Stage 1: router logits
+# --------------------------------------------------------------------------
+def router_logits(h, W_r, b_r=None):
+    """z_t = W_r h_t + b_r for every token.
+
+    [P1] §二 第一步: the router is a small linear layer, W_r in R^{N x d};
+    [P4] "router_logits = x @ W_router^T".
+    h: [T, d], W_r: [N, d], b_r: [N] or None. Returns z: [T, N].
+    """
+    h = np.asarray(h, dtype=np.float64)
+    W_r = np.asarray(W_r, dtype=np.float64)
+    z = h @ W_r.T
+    if b_r is not None:
+        z = z + np.asarray(b_r, dtype=np.float64)[None, :]
+    return z
+
+
+# --------------------------------------------------------------------------
+# Stage 2: scores, selection, gates
+# --------------------------------------------------------------------------
+def softmax(z):
+    """p_{t,i} = exp(z_{t,i}) / sum_j exp(z_{t,j}) over all N experts.
+
+    [P1] §二 第二步. The row maximum is subtracted first; in exact
+    arithmetic this changes nothing.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    m = z.max(axis=-1, keepdims=True)
+    e = np.exp(z - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def sigmoid(z):
+    """sigma(z) = 1 / (1 + exp(-z)), per expert.
+
+    [P2] "最常见的 router": DeepSeek-V3 scores with a sigmoid and then
+    normalises over the selected experts; [P5] §8 lists sigmoid routers.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-z))
+
+
+def scores(z, score_kind):
+    if score_kind == SOFTMAX:
+        return softmax(z)
+    if score_kind == SIGMOID:
+        return sigmoid(z)
+    raise ValueError(f"unknown score kind {score_kind!r}")
+
+
+def select_topk(q, k):
+    """S_t = TopK(q_t, k): the k experts with the largest selection score.
+
+    [P1] §二 第三步. Order: descending q; equal q go to the lower index
+    first (the pages only warn that torch.topk is not stable on ties, [P2]
+    "怎么知道实现没把梯度弄丢"). A stable sort of -q gives exactly this order.
+    q: [T, N]. Returns int64 [T, k].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    if not 1 <= k <= q.shape[-1]:
+        raise ValueError("need 1 <= k <= N")
+    order = np.argsort(-q, axis=-1, kind="stable")
+    return order[:, :k]
+
+
+def gates_from_scores(p, S, norm):
+    """Gate weights of the selected experts, in slot order.
+
+    NORM_SELECTED: g_{t,i} = p_{t,i} / sum_{j in S_t} p_{t,j}  ([P1] §二
+    第三步 formula for g; [P2] sigmoid-then-renormalise).
+    NORM_NONE: g_{t,i} = p_{t,i}, the full-softmax probability of the chosen
+    expert (Switch top-1, [P2] "例如分数为 [2, 1, 0]" paragraph; [P3] §2.1
+    scatter of top_probs with no renormalisation).
+    """
+    ps = np.take_along_axis(np.asarray(p, dtype=np.float64), S, axis=-1)
+    if norm == NORM_SELECTED:
+        return ps / ps.sum(axis=-1, keepdims=True)
+    if norm == NORM_NONE:
+        return ps
+    raise ValueError(f"unknown norm {norm!r}")
+
+
+def gates_from_selected_logits(z, S):
+    """g_i = exp(s_i) / sum_{j in TopK} exp(s_j): softmax over the selected logits.
+
+    [P2] "最常见的 router" formula; the page states it equals a full softmax
+    followed by renormalisation over the selected experts.
+    """
+    zs = np.take_along_axis(np.asarray(z, dtype=np.float64), S, axis=-1)
+    m = zs.max(axis=-1, keepdims=True)
+    e = np.exp(zs - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def route(z, k, score_kind=SOFTMAX, norm=NORM_SELECTED, sel_bias=None):
+    """Scores, selection and gates for every token.
+
+    p = score(z); q = p + bias (bias steers selection only: [P1] §五
+    "动态调整专家选择偏置", [P4] overloaded experts become harder to select,
+    [P5] §7 bias added to router scores); S = TopK(q, k); g from p.
+    Returns (S [T,k] int64, g [T,k], p [T,N], q [T,N]).
+    """
+    p = scores(z, score_kind)
+    q = p if sel_bias is None else p + np.asarray(sel_bias, dtype=np.float64)[None, :]
+    S = select_topk(q, k)
+    g = gates_from_scores(p, S, norm)
+    return S, g, p, q
+
+
+def gate_matrix(S, g, N):
+    """Dense [T, N] gate matrix: g at the selected experts, zero elsewhere.
+
+    [P3] §2.1: gates = zeros_like(probs); gates.scatter_(-1, top_indices, w).
+    """
+    T = S.shape[0]
+    G = np.zeros((T, N), dtype=np.float64)
+    np.put_along_axis(G, S, g, axis=-1)
+    return G
+
+
+# --------------------------------------------------------------------------
+# Stage 3/4: dispatch (regroup (token, slot) pairs by expert)
+# --------------------------------------------------------------------------
+def dispatch(S, N):
+    """Per-expert buckets of the (token, slot) pairs.
+
+    [P1] §三 Token Dispatch: pairs sent to the same expert are gathered
+    together, tokens listed in ascending order (E0 <- T0, T2 ...); [P5] §3
+    stage ② regroups tokens by expert so that each expert runs one GEMM.
+    Returns
+      counts    [N]    tokens per expert,
+      offsets   [N+1]  exclusive prefix sum of counts,
+      row_token [T*k]  token of each dispatched row,
+      inv       [T,k]  dispatched row of (token t, slot j).
+    """
+    S = np.asarray(S)
+    T, k = S.shape
+    e_flat = S.reshape(-1)
+    t_flat = np.repeat(np.arange(T), k)
+    counts = np.bincount(e_flat, minlength=N).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    order = np.lexsort((t_flat, e_flat))      # by expert, then by token
+    row_token = t_flat[order]
+    inv_flat = np.empty(T * k, dtype=np.int64)
+    inv_flat[order] = np.arange(T * k)
+    return counts, offsets, row_token, inv_flat.reshape(T, k)
+
+
+# --------------------------------------------------------------------------
+# Stage 5/6: the expert FFN
+# --------------------------------------------------------------------------
+def silu(a):
+    """SiLU(a) = a * sigma(a)."""
+    a = np.asarray(a, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return a / (1.0 + np.exp(-a))
+
+
+def swiglu_expert(x, W_gate, W_up, W_down):
+    """E(x) = W_down (SiLU(W_gate x) ⊙ W_up x), row by row.
+
+    [P1] §一: FFN(h) = W_down (SiLU(W_gate h) ⊙ W_up h) and the per-expert
+    form E_i(h). x: [R, d], W_gate/W_up: [F, d], W_down: [d, F].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = silu(x @ np.asarray(W_gate, np.float64).T) * (x @ np.asarray(W_up, np.float64).T)
+    return a @ np.asarray(W_down, np.float64).T
+
+
+def swiglu_act(x, W_gate, W_up):
+    """The expert's hidden activation SiLU(W_gate x) ⊙ W_up x, [R, F]."""
+    x = np.asarray(x, dtype=np.float64)
+    return silu(x @ np.asarray(W_gate, np.float64).T) * (x @ np.asarray(W_up, np.float64).T)
+
+
+def expert_rows(x_disp, offsets, W_gate, W_up, W_down):
+    """y_rows[r] = E_e(x_disp[r]) for every dispatched row r of expert e.
+
+    Experts with no rows are skipped ([P1] §十四, [P2] sparse_moe).
+    """
+    R = x_disp.shape[0]
+    y = np.zeros((R, W_down.shape[1]), dtype=np.float64)
+    for e in range(len(offsets) - 1):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            y[r0:r1] = swiglu_expert(x_disp[r0:r1], W_gate[e], W_up[e], W_down[e])
+    return y
+
+
+# --------------------------------------------------------------------------
+# Stage 7: combine
+# --------------------------------------------------------------------------
+def combine(y_rows, inv, g, y_shared=None):
+    """out_t = [y_shared_t +] sum_j g_{t,j} * y_rows[inv[t, j]].
+
+    [P2] "选好以后": outputs are weighted and ADDED back to their token,
+    never overwritten or concatenated; [P5] §3 stage ④ restores token order
+    and fuses by router weight; [P1] §八 adds the shared experts' output.
+    """
+    y_rows = np.asarray(y_rows, dtype=np.float64)
+    inv = np.asarray(inv)
+    T, k = inv.shape
+    out = np.zeros((T, y_rows.shape[1]), dtype=np.float64)
+    if y_shared is not None:
+        out += np.asarray(y_shared, dtype=np.float64)
+    for j in range(k):
+        out += np.asarray(g, np.float64)[:, j:j + 1] * y_rows[inv[:, j]]
+    return out
+
+
+# --------------------------------------------------------------------------
+# The whole layer
+# --------------------------------------------------------------------------
+def moe_forward(h, W_r, W_gate, W_up, W_down, k, score_kind=SOFTMAX,
+                norm=NORM_SELECTED, sel_bias=None, b_r=None, shared=None):
+    """Sparse forward, one expert at a time.
+
+    Follows the per-expert loop of [P1] §十四 and [P2] sparse_moe: route,
+    then for every expert gather its tokens, run the expert, weight by the
+    gate and index-add into the output; plus the always-on shared expert of
+    [P1] §八: y_t = sum_{s in Shared} E_s(h_t) + sum_{i in S_t} g_{t,i} E_i(h_t).
+    ``shared`` is None or a tuple (Ws_gate, Ws_up, Ws_down).
+    Returns (y [T,d], z [T,N], S [T,k], g [T,k]).
+    """
+    h = np.asarray(h, dtype=np.float64)
+    z = router_logits(h, W_r, b_r)
+    S, g, _, _ = route(z, k, score_kind, norm, sel_bias)
+    y = np.zeros_like(h)
+    if shared is not None:
+        y += swiglu_expert(h, *shared)
+    for e in range(W_gate.shape[0]):
+        tok, slot = np.nonzero(S == e)
+        if tok.size == 0:
+            continue
+        y_e = swiglu_expert(h[tok], W_gate[e], W_up[e], W_down[e])
+        np.add.at(y, tok, g[tok, slot][:, None] * y_e)
+    return y, z, S, g
+
+
+def moe_forward_dense(h, W_r, W_gate, W_up, W_down, k, score_kind=SOFTMAX,
+                      norm=NORM_SELECTED, sel_bias=None, b_r=None, shared=None):
+    """Dense masked forward: every expert runs on every token.
+
+    [P2] "怎么知道实现没把梯度弄丢": let all experts process all inputs, set
+    the weight of unselected experts to zero, and sum; it must equal the
+    sparse dispatch result. The gate matrix is [P3] §2.1's scattered gates.
+    """
+    h = np.asarray(h, dtype=np.float64)
+    z = router_logits(h, W_r, b_r)
+    S, g, _, _ = route(z, k, score_kind, norm, sel_bias)
+    G = gate_matrix(S, g, W_gate.shape[0])
+    y = np.zeros_like(h)
+    if shared is not None:
+        y += swiglu_expert(h, *shared)
+    for e in range(W_gate.shape[0]):
+        y += G[:, e:e + 1] * swiglu_expert(h, W_gate[e], W_up[e], W_down[e])
+    return y, z, S, g
+
+
+# --------------------------------------------------------------------------
+# Brute-force helpers used only by the oracle's own pins
+# --------------------------------------------------------------------------
+def topk_by_rank_count(q_row, k):
+    """Selection by counting, without sorting: expert i is selected iff fewer
+    than k experts beat it, where j beats i when q_j > q_i, or q_j == q_i and
+    j < i. Returns the selected indices ordered by that same relation."""
+    q_row = list(map(float, q_row))
+    N = len(q_row)
+    beats = lambda j, i: q_row[j] > q_row[i] or (q_row[j] == q_row[i] and j < i)
+    rank = [sum(1 for j in range(N) if j != i and beats(j, i)) for i in range(N)]
+    chosen = [i for i in range(N) if rank[i] < k]
+    return sorted(chosen, key=lambda i: rank[i])
+
+
+def topk_by_subsets(q_row, k):
+    """Exhaustive: the k-subset with the largest score sum; among equal sums
+    the lexicographically smallest index tuple. Valid as a pin only when the
+    scores of different subsets do not tie."""
+    best = None
+    for sub in itertools.combinations(range(len(q_row)), k):
+        key = (-sum(float(q_row[i]) for i in sub), sub)
+        if best is None or key < best:
+            best = key
+    return set(best[1])

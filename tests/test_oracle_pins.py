@@ -1,0 +1,406 @@
+"""Pins for the CPU oracle: worked examples printed on the pages, closed forms,
+library routines and brute force. CPU only (no GPU marker).
+
+A mistake anywhere in the oracle (a dropped term, a wrong sign or index, a
+transposed operand, an overwrite instead of an add) fails at least one test
+here; the mutation tests at the end plant such mistakes in the oracle and
+check that the pins catch them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as Fnn
+
+from conftest import load_golden
+from oracle import moe_oracle as O
+
+
+# ---------------------------------------------------------------- router ---
+def test_router_logits_vs_library_linear():
+    rng = np.random.default_rng(1)
+    h = rng.standard_normal((7, 5))
+    W = rng.standard_normal((3, 5))
+    b = rng.standard_normal(3)
+    ref = Fnn.linear(torch.from_numpy(h), torch.from_numpy(W), torch.from_numpy(b)).numpy()
+    np.testing.assert_allclose(O.router_logits(h, W, b), ref, rtol=0, atol=1e-12)
+    ref0 = Fnn.linear(torch.from_numpy(h), torch.from_numpy(W)).numpy()
+    np.testing.assert_allclose(O.router_logits(h, W), ref0, rtol=0, atol=1e-12)
+    # orientation: logit i is row i of W_r dotted with h (not a column)
+    h1 = np.array([[1.0, 0.0, 0.0, 0.0, 0.0]])
+    np.testing.assert_array_equal(O.router_logits(h1, W)[0], W[:, 0])
+
+
+# ----------------------------------------------------------------- scores ---
+def test_page1_softmax_example():
+    g = load_golden("page1_softmax_example.json")
+    z = np.array([g["logits"]])
+    tol = g["printed_abs_tol"]
+    p = O.softmax(z)
+    np.testing.assert_allclose(p[0], g["softmax_printed"], atol=tol, rtol=0)
+    S, gates, _, _ = O.route(z, g["k"], O.SOFTMAX, O.NORM_SELECTED)
+    assert S[0].tolist() == g["selected"]
+    np.testing.assert_allclose(gates[0], g["gates_printed"], atol=tol, rtol=0)
+    np.testing.assert_allclose(O.gates_from_selected_logits(z, S)[0],
+                               g["gates_printed"], atol=tol, rtol=0)
+
+
+def test_page2_selected_renorm_example():
+    g = load_golden("page2_selected_renorm_example.json")
+    z = np.array([g["scores"]])
+    S, gates, _, _ = O.route(z, g["k"], O.SOFTMAX, O.NORM_SELECTED)
+    assert S[0].tolist() == g["selected"]
+    np.testing.assert_allclose(gates[0], g["gates_printed"], atol=g["printed_abs_tol"], rtol=0)
+    # closed form: e^2 / (e^2 + e^1) = 1 / (1 + e^-1)
+    assert abs(gates[0, 0] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+
+
+def test_softmax_vs_library_and_closed_forms():
+    rng = np.random.default_rng(2)
+    z = rng.standard_normal((11, 9)) * 3
+    np.testing.assert_allclose(O.softmax(z), torch.softmax(torch.from_numpy(z), -1).numpy(),
+                               atol=1e-15, rtol=0)
+    np.testing.assert_allclose(O.softmax(np.zeros((1, 8))), np.full((1, 8), 1 / 8), atol=1e-15)
+    a = 0.7
+    p = O.softmax(np.array([[a, 0.0]]))
+    assert abs(p[0, 0] - 1 / (1 + math.exp(-a))) < 1e-15
+    # large logits do not overflow
+    assert np.isfinite(O.softmax(np.array([[1000.0, 999.0]]))).all()
+
+
+def test_sigmoid_vs_library_and_closed_forms():
+    rng = np.random.default_rng(3)
+    z = rng.standard_normal((5, 6)) * 4
+    np.testing.assert_allclose(O.sigmoid(z), torch.sigmoid(torch.from_numpy(z)).numpy(),
+                               atol=1e-15, rtol=0)
+    assert O.sigmoid(np.array([0.0]))[0] == 0.5
+    assert abs(O.sigmoid(np.array([math.log(3.0)]))[0] - 0.75) < 1e-15
+    assert O.sigmoid(np.array([-800.0]))[0] == 0.0
+
+
+def test_renorm_identity_softmax_then_renorm_equals_topk_then_softmax():
+    rng = np.random.default_rng(4)
+    for k in (1, 2, 3, 8):
+        z = rng.standard_normal((50, 16)) * 2
+        S = O.select_topk(z, k)
+        a = O.gates_from_scores(O.softmax(z), S, O.NORM_SELECTED)
+        b = O.gates_from_selected_logits(z, S)
+        np.testing.assert_allclose(a, b, atol=1e-12, rtol=0)
+        np.testing.assert_allclose(a.sum(-1), 1.0, atol=1e-12)
+
+
+# -------------------------------------------------------------- selection ---
+def test_topk_ties_go_to_lower_index():
+    q = np.array([[1.0, 3.0, 3.0, 2.0, 3.0]])
+    assert O.select_topk(q, 1)[0].tolist() == [1]
+    assert O.select_topk(q, 2)[0].tolist() == [1, 2]
+    assert O.select_topk(q, 3)[0].tolist() == [1, 2, 4]
+    assert O.select_topk(q, 5)[0].tolist() == [1, 2, 4, 3, 0]
+    q0 = np.zeros((1, 6))
+    assert O.select_topk(q0, 3)[0].tolist() == [0, 1, 2]
+
+
+def test_topk_vs_rank_counting_brute_force():
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        N = int(rng.integers(1, 9))
+        k = int(rng.integers(1, N + 1))
+        q = np.round(rng.standard_normal(N) * 2) / 2   # many exact ties
+        assert O.select_topk(q[None], k)[0].tolist() == O.topk_by_rank_count(q, k)
+
+
+def test_topk_vs_subset_brute_force_and_library():
+    rng = np.random.default_rng(6)
+    for _ in range(200):
+        N = int(rng.integers(1, 8))
+        k = int(rng.integers(1, N + 1))
+        q = rng.standard_normal(N)          # continuous: no ties
+        S = O.select_topk(q[None], k)[0]
+        assert set(S.tolist()) == O.topk_by_subsets(q, k)
+        tv, ti = torch.topk(torch.from_numpy(q), k)
+        assert S.tolist() == ti.tolist()
+
+
+def test_switch_top1_keeps_full_softmax_probability():
+    rng = np.random.default_rng(7)
+    z = rng.standard_normal((20, 6))
+    S, g, p, _ = O.route(z, 1, O.SOFTMAX, O.NORM_NONE)
+    np.testing.assert_allclose(g[:, 0], p.max(-1), atol=0)
+    assert (g[:, 0] >= 1 / 6 - 1e-15).all() and (g[:, 0] < 1).all()
+    # with renormalisation a top-1 gate would be exactly 1
+    _, g1, _, _ = O.route(z, 1, O.SOFTMAX, O.NORM_SELECTED)
+    np.testing.assert_array_equal(g1, 1.0)
+    # one expert: the gate is 1 either way
+    _, gN1, _, _ = O.route(z[:, :1], 1, O.SOFTMAX, O.NORM_NONE)
+    np.testing.assert_array_equal(gN1, 1.0)
+
+
+def test_k_equals_N_gates_are_the_probabilities():
+    rng = np.random.default_rng(8)
+    z = rng.standard_normal((10, 5))
+    S, g, p, _ = O.route(z, 5, O.SOFTMAX, O.NORM_SELECTED)
+    np.testing.assert_allclose(g, np.take_along_axis(p, S, -1), atol=1e-15)
+    np.testing.assert_allclose(g.sum(-1), 1.0, atol=1e-15)
+
+
+def test_sigmoid_bias_steers_selection_not_gates():
+    z = np.array([[2.0, 0.0, -1.0]])
+    bias = np.array([0.0, 0.0, 10.0])
+    S, g, p, q = O.route(z, 2, O.SIGMOID, O.NORM_SELECTED, bias)
+    assert S[0].tolist() == [2, 0]
+    s2, s0 = 1 / (1 + math.exp(1.0)), 1 / (1 + math.exp(-2.0))
+    np.testing.assert_allclose(g[0], [s2 / (s2 + s0), s0 / (s2 + s0)], atol=1e-15)
+    # without the bias expert 1 (sigma(0) = 0.5) beats expert 2
+    S0, _, _, _ = O.route(z, 2, O.SIGMOID, O.NORM_SELECTED)
+    assert S0[0].tolist() == [0, 1]
+    # NORM_NONE keeps the raw sigmoid scores
+    _, gn, _, _ = O.route(z, 2, O.SIGMOID, O.NORM_NONE, bias)
+    np.testing.assert_allclose(gn[0], [s2, s0], atol=1e-15)
+
+
+def test_sigmoid_bias_brute_force():
+    rng = np.random.default_rng(9)
+    for _ in range(200):
+        N = int(rng.integers(2, 9))
+        k = int(rng.integers(1, N + 1))
+        z = rng.standard_normal(N) * 2
+        b = rng.standard_normal(N) * 0.3
+        S, g, _, _ = O.route(z[None], k, O.SIGMOID, O.NORM_SELECTED, b)
+        sig = [1 / (1 + math.exp(-v)) for v in z]
+        q = [sig[i] + b[i] for i in range(N)]
+        assert S[0].tolist() == O.topk_by_rank_count(q, k)
+        tot = sum(sig[i] for i in S[0])
+        np.testing.assert_allclose(g[0], [sig[i] / tot for i in S[0]], atol=1e-14)
+
+
+def test_gate_matrix_matches_scatter():
+    rng = np.random.default_rng(10)
+    z = rng.standard_normal((6, 5))
+    S, g, _, _ = O.route(z, 2)
+    G = O.gate_matrix(S, g, 5)
+    ref = torch.zeros(6, 5, dtype=torch.float64).scatter_(
+        -1, torch.from_numpy(S), torch.from_numpy(g)).numpy()
+    np.testing.assert_array_equal(G, ref)
+
+
+# --------------------------------------------------------------- dispatch ---
+def _choices(golden):
+    S = np.array([[e for e, _ in row] for row in golden["choices"]])
+    g = np.array([[w for _, w in row] for row in golden["choices"]])
+    return S, g
+
+
+def test_page1_dispatch_table():
+    gd = load_golden("page1_dispatch_table.json")
+    S, _ = _choices(gd)
+    counts, offsets, row_token, inv = O.dispatch(S, gd["N"])
+    assert counts.tolist() == gd["counts"]
+    assert offsets.tolist() == gd["offsets"]
+    for e, toks in gd["buckets"].items():
+        e = int(e)
+        assert row_token[offsets[e]:offsets[e + 1]].tolist() == toks
+    for t in range(S.shape[0]):
+        for j in range(S.shape[1]):
+            r = inv[t, j]
+            assert row_token[r] == t and offsets[S[t, j]] <= r < offsets[S[t, j] + 1]
+
+
+def test_dispatch_brute_force():
+    rng = np.random.default_rng(11)
+    for _ in range(50):
+        N = int(rng.integers(1, 10))
+        k = int(rng.integers(1, N + 1))
+        T = int(rng.integers(0, 40))
+        S = np.array([rng.permutation(N)[:k] for _ in range(T)]).reshape(T, k)
+        counts, offsets, row_token, inv = O.dispatch(S, N)
+        pairs = sorted((int(S[t, j]), t, j) for t in range(T) for j in range(k))
+        assert row_token.tolist() == [t for _, t, _ in pairs]
+        for r, (e, t, j) in enumerate(pairs):
+            assert inv[t, j] == r
+        assert counts.sum() == T * k
+        assert counts.tolist() == [sum(1 for p in pairs if p[0] == e) for e in range(N)]
+
+
+# ------------------------------------------------------------- expert FFN ---
+def test_swiglu_vs_library():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((9, 6))
+    Wg, Wu, Wd = rng.standard_normal((5, 6)), rng.standard_normal((5, 6)), rng.standard_normal((6, 5))
+    tx, tg, tu, td = map(torch.from_numpy, (x, Wg, Wu, Wd))
+    ref = Fnn.linear(Fnn.silu(Fnn.linear(tx, tg)) * Fnn.linear(tx, tu), td).numpy()
+    np.testing.assert_allclose(O.swiglu_expert(x, Wg, Wu, Wd), ref, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(O.silu(x), Fnn.silu(tx).numpy(), atol=1e-15, rtol=0)
+
+
+def test_swiglu_scalar_closed_form():
+    a, b, c = 1.3, -0.4, 2.5
+    y = O.swiglu_expert(np.array([[1.0]]), np.array([[a]]), np.array([[b]]), np.array([[c]]))
+    assert abs(y[0, 0] - c * (a / (1 + math.exp(-a))) * b) < 1e-15
+    # gate branch is the SiLU one: swapping W_gate and W_up changes the result
+    y2 = O.swiglu_expert(np.array([[1.0]]), np.array([[b]]), np.array([[a]]), np.array([[c]]))
+    assert abs(y2[0, 0] - y[0, 0]) > 1e-3
+
+
+# ---------------------------------------------------------------- combine ---
+def test_page2_combine_example():
+    gd = load_golden("page2_combine_example.json")
+    S, g = _choices(gd)
+    counts, offsets, row_token, inv = O.dispatch(S, gd["N"])
+    y_rows = np.zeros((S.size, 2))
+    for t in range(S.shape[0]):
+        for j in range(S.shape[1]):
+            y_rows[inv[t, j]] = gd["expert_outputs"][f"{t}:{S[t, j]}"]
+    # dispatch regrouping of the page: expert 2 receives both tokens
+    assert counts.tolist() == [1, 1, 2]
+    out = O.combine(y_rows, inv, g)
+    np.testing.assert_allclose(out, gd["y_printed"], atol=1e-12, rtol=0)
+
+
+def test_combine_with_shared_and_zero_gates():
+    rng = np.random.default_rng(13)
+    y_rows = rng.standard_normal((6, 4))
+    inv = np.array([[0, 3], [1, 4], [2, 5]])
+    ysh = rng.standard_normal((3, 4))
+    g = np.zeros((3, 2))
+    np.testing.assert_array_equal(O.combine(y_rows, inv, g, ysh), ysh)
+    g1 = np.array([[1.0, 0.0], [0.0, 1.0], [0.5, 0.5]])
+    out = O.combine(y_rows, inv, g1)
+    np.testing.assert_allclose(out[0], y_rows[0]); np.testing.assert_allclose(out[1], y_rows[4])
+    np.testing.assert_allclose(out[2], 0.5 * (y_rows[2] + y_rows[5]))
+
+
+# ------------------------------------------------------------ whole layer ---
+def _tiny(rng, T, d, N, F, shared=False, F_sh=3):
+    h = rng.standard_normal((T, d))
+    W_r = rng.standard_normal((N, d))
+    Wg = rng.standard_normal((N, F, d)); Wu = rng.standard_normal((N, F, d))
+    Wd = rng.standard_normal((N, d, F))
+    sh = None
+    if shared:
+        sh = (rng.standard_normal((F_sh, d)), rng.standard_normal((F_sh, d)),
+              rng.standard_normal((d, F_sh)))
+    return h, W_r, Wg, Wu, Wd, sh
+
+
+@pytest.mark.parametrize("score", [O.SOFTMAX, O.SIGMOID])
+@pytest.mark.parametrize("norm", [O.NORM_SELECTED, O.NORM_NONE])
+@pytest.mark.parametrize("use_bias", [False, True])
+@pytest.mark.parametrize("shared", [False, True])
+def test_sparse_equals_dense_masked(score, norm, use_bias, shared):
+    rng = np.random.default_rng(14)
+    for _ in range(4):
+        T, d, N, F = int(rng.integers(1, 17)), int(rng.integers(1, 9)), int(rng.integers(1, 7)), int(rng.integers(1, 6))
+        k = int(rng.integers(1, N + 1))
+        h, W_r, Wg, Wu, Wd, sh = _tiny(rng, T, d, N, F, shared)
+        bias = rng.standard_normal(N) * 0.2 if use_bias else None
+        ys, z, S, g = O.moe_forward(h, W_r, Wg, Wu, Wd, k, score, norm, bias, shared=sh)
+        yd, _, _, _ = O.moe_forward_dense(h, W_r, Wg, Wu, Wd, k, score, norm, bias, shared=sh)
+        np.testing.assert_allclose(ys, yd, atol=1e-12, rtol=1e-12)
+
+
+def test_single_expert_is_dense_swiglu_ffn():
+    rng = np.random.default_rng(15)
+    h, W_r, Wg, Wu, Wd, _ = _tiny(rng, 12, 6, 1, 5)
+    y, _, S, g = O.moe_forward(h, W_r, Wg, Wu, Wd, 1)
+    th = torch.from_numpy(h)
+    ref = Fnn.linear(Fnn.silu(Fnn.linear(th, torch.from_numpy(Wg[0]))) *
+                     Fnn.linear(th, torch.from_numpy(Wu[0])), torch.from_numpy(Wd[0])).numpy()
+    np.testing.assert_allclose(y, ref, atol=1e-12, rtol=0)
+    assert (S == 0).all() and (g == 1).all()
+
+
+def test_shared_expert_alone_when_routed_outputs_vanish():
+    rng = np.random.default_rng(16)
+    h, W_r, Wg, Wu, Wd, sh = _tiny(rng, 10, 6, 4, 5, shared=True, F_sh=7)
+    Wd0 = np.zeros_like(Wd)
+    y, _, _, _ = O.moe_forward(h, W_r, Wg, Wu, Wd0, 2, shared=sh)
+    th = torch.from_numpy(h)
+    ref = Fnn.linear(Fnn.silu(Fnn.linear(th, torch.from_numpy(sh[0]))) *
+                     Fnn.linear(th, torch.from_numpy(sh[1])), torch.from_numpy(sh[2])).numpy()
+    np.testing.assert_allclose(y, ref, atol=1e-12, rtol=0)
+
+
+def test_stagewise_composition_equals_layer():
+    """route -> dispatch -> expert_rows -> combine equals moe_forward."""
+    rng = np.random.default_rng(17)
+    h, W_r, Wg, Wu, Wd, sh = _tiny(rng, 15, 6, 5, 4, shared=True)
+    bias = rng.standard_normal(5) * 0.1
+    y, z, S, g = O.moe_forward(h, W_r, Wg, Wu, Wd, 3, O.SIGMOID, O.NORM_SELECTED, bias, shared=sh)
+    counts, offsets, row_token, inv = O.dispatch(S, 5)
+    y_rows = O.expert_rows(h[row_token], offsets, Wg, Wu, Wd)
+    out = O.combine(y_rows, inv, g, O.swiglu_expert(h, *sh))
+    np.testing.assert_allclose(out, y, atol=1e-12, rtol=0)
+
+
+def test_page1_worked_output_weights():
+    """The page's y_t = 0.599 E0 + 0.401 E2 with E_i replaced by unit vectors."""
+    g = load_golden("page1_softmax_example.json")
+    z = np.array([g["logits"]])
+    S, gates, _, _ = O.route(z, 2)
+    counts, offsets, row_token, inv = O.dispatch(S, 4)
+    y_rows = np.zeros((2, 4))
+    for j in range(2):
+        y_rows[inv[0, j], S[0, j]] = 1.0        # E_i(h) = e_i
+    out = O.combine(y_rows, inv, gates)
+    np.testing.assert_allclose(out[0], [0.599, 0, 0.401, 0], atol=5e-4)
+
+
+# ------------------------------------------------- mutation: pins catch bugs ---
+def _run_pins_expect_failure(monkeypatch, name, bad, pins):
+    monkeypatch.setattr(O, name, bad)
+    failed = 0
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, f"a planted mistake in {name} went unnoticed"
+
+
+def test_mutation_overwrite_instead_of_add(monkeypatch):
+    def bad_combine(y_rows, inv, g, y_shared=None):
+        out = np.zeros((inv.shape[0], y_rows.shape[1]))
+        for j in range(inv.shape[1]):
+            out = g[:, j:j + 1] * y_rows[inv[:, j]]          # overwrite
+        return out
+    _run_pins_expect_failure(monkeypatch, "combine", bad_combine, [test_page2_combine_example])
+
+
+def test_mutation_transposed_gate_up(monkeypatch):
+    def bad_swiglu(x, Wg, Wu, Wd):
+        return (O.silu(x @ np.asarray(Wu).T) * (x @ np.asarray(Wg).T)) @ np.asarray(Wd).T
+    _run_pins_expect_failure(monkeypatch, "swiglu_expert", bad_swiglu,
+                             [test_swiglu_vs_library, test_swiglu_scalar_closed_form])
+
+
+def test_mutation_tie_break_to_higher_index(monkeypatch):
+    def bad_topk(q, k):
+        q = np.asarray(q, dtype=np.float64)
+        order = np.argsort(-q[:, ::-1], axis=-1, kind="stable")
+        return (q.shape[-1] - 1 - order)[:, :k]
+    _run_pins_expect_failure(monkeypatch, "select_topk", bad_topk,
+                             [test_topk_ties_go_to_lower_index])
+
+
+def test_mutation_bias_in_gates(monkeypatch):
+    orig = O.gates_from_scores
+    def bad_route(z, k, score_kind=O.SOFTMAX, norm=O.NORM_SELECTED, sel_bias=None):
+        p = O.scores(z, score_kind)
+        q = p if sel_bias is None else p + np.asarray(sel_bias)[None, :]
+        S = O.select_topk(q, k)
+        return S, orig(q, S, norm), p, q                      # gates from q
+    _run_pins_expect_failure(monkeypatch, "route", bad_route,
+                             [test_sigmoid_bias_steers_selection_not_gates])
+
+
+def test_mutation_dispatch_unstable_order(monkeypatch):
+    def bad_dispatch(S, N):
+        T, k = S.shape
+        e_flat = S.reshape(-1); t_flat = np.repeat(np.arange(T), k)
+        counts = np.bincount(e_flat, minlength=N)
+        offsets = np.concatenate([[0], np.cumsum(counts)])
+        order = np.lexsort((-t_flat, e_flat))                  # tokens descending
+        inv = np.empty(T * k, dtype=np.int64); inv[order] = np.arange(T * k)
+        return counts, offsets, t_flat[order], inv.reshape(T, k)
+    _run_pins_expect_failure(monkeypatch, "dispatch", bad_dispatch, [test_page1_dispatch_table])
