@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE-layer forward on B300: tokens/s of one moe_forward per
+step on a fixed synthetic batch, the grouped-GEMM roofline fraction, the
+end-to-end rate through the C ABI with host buffers, and the CPU oracle timed
+on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+N > 1 runs under torchrun, one replica per GPU (tokens are independent, so
+every rank runs its own batch with its own copy of the weights and no
+collective touches the data path); the timing is the max over ranks.
+Prints ONE JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from top_routing_grouped_bias_b300 import api, synth  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s; grouped-GEMM TFLOP/s & HBM GB/s vs B300 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+KERNELS_PER_FORWARD = 7  # route 1, dispatch 3, grouped GEMM 2, combine 1
+
+
+# ------------------------------------------------------------ host logic ---
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar (timing only; no data-path collective)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(units_per_rank: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units all ranks processed / the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_work(w):
+    """Algorithmic FLOPs and bytes of one forward (touched experts only)."""
+    e = 4 if w.dtype == "f32" else 2
+    R = w.T * w.k
+    gemm_flops = 2.0 * 3 * w.d * w.F * R + 2.0 * 3 * w.d * w.F_sh * w.T
+    router_flops = 2.0 * w.N * w.d * w.T
+    return dict(gemm_flops=gemm_flops, router_flops=router_flops, R=R, e=e)
+
+
+def gemm_bytes(w, counts):
+    """Algorithmic HBM bytes of the grouped GEMM pair: each touched expert's
+    weights once, activations in and out once per pass."""
+    e = 4 if w.dtype == "f32" else 2
+    touched = int((np.asarray(counts) > 0).sum())
+    R = w.T * w.k
+    b = touched * 3 * w.d * w.F * e
+    b += R * (w.d + w.F) * e + R * (w.F + w.d) * e
+    if w.F_sh:
+        b += 3 * w.d * w.F_sh * e + w.T * (w.d + w.F_sh) * e * 2
+    return b
+
+
+def traffic_from_profile(workload: str):
+    """DRAM traffic per grouped-GEMM stage from the committed ncu summary, or
+    None when the summary is missing or the kernel source changed since."""
+    p = os.path.join(ROOT, "profiles", f"grouped_gemm_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p, encoding="utf-8").read()
+    m = re.search(r"dram_bytes_per_stage:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{16,64})", txt)
+    if not m or not h:
+        return None
+    src = os.path.join(ROOT, "top_routing_grouped_bias_b300", "csrc", "grouped_gemm.cu")
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if not cur.startswith(h.group(1)):
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        loaded = [r for r in rows if r["power"] > 200] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([r["sm"] for r in loaded])),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(loaded), "power_w_max": max(r["power"] for r in rows)}
+
+
+# --------------------------------------------------------- CPU baseline ---
+def oracle_sample(w, n_tokens: int, seed: int = 0):
+    """Inputs of a bounded sample of the workload for the CPU oracle: the
+    workload's own weights (drawn with the same generator as the GPU run) and
+    its first n_tokens tokens."""
+    inp = synth.make_inputs(w, seed=seed, device="cuda" if torch.cuda.is_available() else "cpu")
+    f32 = lambda t: None if t is None else t.float().cpu().numpy()
+    s = dict(h=f32(inp["h"][:n_tokens]), W_r=f32(inp["W_r"]), W_gate=f32(inp["W_gate"]),
+             W_up=f32(inp["W_up"]), W_down=f32(inp["W_down"]), sel_bias=f32(inp["sel_bias"]))
+    s["shared"] = None
+    if w.F_sh > 0:
+        s["shared"] = (f32(inp["Ws_gate"]), f32(inp["Ws_up"]), f32(inp["Ws_down"]))
+    del inp
+    if torch.cuda.is_available():
+        torch.cuda.empty_cache()
+    return s
+
+
+def run_oracle(w, s):
+    from oracle import moe_oracle as O
+    return O.moe_forward(s["h"], s["W_r"], s["W_gate"], s["W_up"], s["W_down"], w.k, w.score,
+                         w.norm, s["sel_bias"], shared=s["shared"])
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+SAMPLE_TOKENS = {"tiny_fp32": 64, "mixtral_prefill": 96, "mixtral_decode": 16,
+                 "fine_grained_shared": 24, "switch_top1": 2048}
+
+
+def cpu_baseline(w, steps: int = 1):
+    n = min(w.T, SAMPLE_TOKENS.get(w.name, 64))
+    s = oracle_sample(w, n)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run_oracle(w, s)
+    dt = time.perf_counter() - t0
+    return {"value": n * steps / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens of {w.name} (all {w.N} experts' weights), fp64 numpy, "
+                      f"{steps} step(s), {dt:.2f} s"}
+
+
+# ------------------------------------------------------------ our arm ---
+def bench_ours(args, w):
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    api.load()
+    cfg = api.config_for(w)
+    inp = synth.make_inputs(w, seed=0, device=dev)
+    tdt = w.torch_dtype
+    ws = api.alloc_workspace(cfg, dev)
+    outs = api.alloc_outputs(cfg, dev, tdt, logits=False)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        api.forward(cfg, inp, outs, ws, stream)
+    torch.cuda.synchronize(dev)
+    assert api.read_status(ws) == api.MOE_OK
+
+    # ---- device-resident timing ----
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            api.forward(cfg, inp, outs, ws, stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    assert api.read_status(ws) == api.MOE_OK
+    ms_max = max_over_ranks(ms, world, dev)
+    value = aggregate_rate(w.T * args.steps, world, ms_max * args.steps / 1e3)
+
+    # ---- grouped-GEMM stage alone (both passes), on the same stream ----
+    counts = outs["counts"].cpu().numpy()
+    R = w.T * w.k
+    idx, gate = outs["idx"], outs["gate"]
+    st = {n: torch.empty(s, dtype=torch.int32, device=dev) for n, s in
+          (("counts", (w.N,)), ("offsets", (w.N + 1,)), ("row_token", (R,)), ("inv", (R,)))}
+    x_disp = torch.empty((R, w.d), dtype=tdt, device=dev)
+    y_rows = torch.empty((R, w.d), dtype=tdt, device=dev)
+    y_sh = torch.empty((w.T, w.d), dtype=tdt, device=dev) if w.F_sh else None
+    api.moe_dispatch(cfg, inp["h"], idx, st["counts"], st["offsets"], st["row_token"], st["inv"],
+                     x_disp, ws, stream)
+
+    def ffn():
+        api.moe_expert_ffn(cfg, x_disp, st["offsets"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                           y_rows, inp["h"], inp.get("Ws_gate"), inp.get("Ws_up"),
+                           inp.get("Ws_down"), y_sh, ws, stream)
+
+    def stage_ms(fn, reps):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    reps = max(args.steps, 5)
+    ffn_ms = stage_ms(ffn, reps)
+    logits_scratch = None
+    route_ms = stage_ms(lambda: api.moe_route(cfg, inp["h"], inp["W_r"], None, inp["sel_bias"],
+                                              None, logits_scratch, idx, gate, ws, stream), reps)
+    disp_ms = stage_ms(lambda: api.moe_dispatch(cfg, inp["h"], idx, st["counts"], st["offsets"],
+                                                st["row_token"], st["inv"], x_disp, ws, stream),
+                       reps)
+    comb_ms = stage_ms(lambda: api.moe_combine(cfg, y_rows, st["inv"], gate, y_sh, outs["out"],
+                                               stream), reps)
+    assert api.read_status(ws) == api.MOE_OK
+
+    # ---- end to end through the C ABI with host buffers ----
+    h_host = inp["h"].cpu().pin_memory()
+    out_host = torch.empty((w.T, w.d), dtype=tdt).pin_memory()
+    h_dev = torch.empty_like(inp["h"])
+    inp_e2e = dict(inp)
+    inp_e2e["h"] = h_dev
+
+    def e2e_step():
+        h_dev.copy_(h_host, non_blocking=True)
+        api.forward(cfg, inp_e2e, outs, ws, stream)
+        out_host.copy_(outs["out"], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    e2e_value = aggregate_rate(w.T * args.steps, world, e2e_ms * args.steps / 1e3)
+
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    work = workload_work(w)
+    gb = gemm_bytes(w, counts)
+    gemm_tflops = work["gemm_flops"] / (ffn_ms * 1e-3) / 1e12
+    gemm_gbs = gb / (ffn_ms * 1e-3) / 1e9
+    tensor_bound = w.T * w.k / max(1, int((counts > 0).sum())) >= 64
+    traffic = traffic_from_profile(w.name)
+    if tensor_bound:
+        peak = peaks["bf16_tflops"]
+        if w.dtype == "f32":
+            peak = peaks["bf16_tflops"] / 2.0   # tf32 nominal rate is half of bf16
+        roof = {"bound": "tensor", "achieved": round(gemm_tflops, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(gemm_tflops / peak, 4), "traffic": traffic}
+    else:
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(gemm_gbs / peak, 4), "traffic": traffic}
+    roof.update({"kernel": "grouped GEMM pair (gate/up SwiGLU + down), one moe_expert_ffn call",
+                 "algorithmic_flops": work["gemm_flops"], "algorithmic_bytes": gb,
+                 "avg_ms": round(ffn_ms, 4), "peak_source": f"{peak_src} (burst)"})
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) hidden, N(0,std) weights; no dataset)",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "ffn": w.F, "k": w.k,
+                   "ffn_shared": w.F_sh, "score": w.score, "norm": w.norm,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (expert weights %.2f GB per step)"
+                         % (3 * w.N * w.d * w.F * (4 if w.dtype == 'f32' else 2) / 1e9)},
+        "roofline": roof,
+        "stages_ms": {"route": round(route_ms, 4), "dispatch": round(disp_ms, 4),
+                      "grouped_gemm": round(ffn_ms, 4), "combine": round(comb_ms, 4)},
+        "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h_host.numel() * h_host.element_size()),
+                "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
+        "clocks": clk.summary(),
+    }
+    return line
+
+
+def bench_reference(args, w):
+    """The CPU oracle as the reference arm, on bounded samples of the workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    n = min(w.T, SAMPLE_TOKENS.get(w.name, 64))
+    s = oracle_sample(w, n)
+    for _ in range(args.warmup):
+        run_oracle(w, s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle(w, s)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    sample = f"{n} of {w.T} tokens of {w.name} per step, fp64 numpy oracle"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "ffn": w.F, "k": w.k,
+                   "ffn_shared": w.F_sh, "score": w.score, "norm": w.norm},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mixtral_prefill", choices=list(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        line = bench_reference(args, w)
+    else:
+        line = bench_ours(args, w)
+        if line is not None:
+            line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(w)
+    rank, world, _ = dist_env()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/*
+ * moe.h -- C ABI of libmoe_b300.so: the forward pass of a token-choice top-k
+ * Mixture-of-Experts SwiGLU FFN layer on one B300 (sm_103a).
+ *
+ * The layer, as the pages define it:
+ *   route    z = W_r h (+ b_r); p = softmax(z) or sigmoid(z); q = p + bias;
+ *            S = TopK(q, k); g = p_S / sum(p_S) (or g = p_S, Switch style)
+ *   dispatch regroup the (token, slot) pairs by expert
+ *   experts  E_i(x) = W_down_i (SiLU(W_gate_i x) * W_up_i x), one grouped GEMM
+ *   combine  y_t = sum_shared E_s(h_t) + sum_{i in S_t} g_{t,i} E_i(h_t)
+ *
+ * Pages cited (title, section):
+ *   [P1] "MOE 专家选择与路由机制"            [P2] "MoE：router 怎样选 expert"
+ *   [P3] pwwt.cn MoE blog, §2.1 Top-K      [P4] "拆解 MoE：单个 Token 如何经过专家层"
+ *   [P5] "【大模型】MoE（专家混合模型）简介"
+ *
+ * Conventions shared by every entry point
+ *   Memory     All tensor pointers are DEVICE pointers, row-major and contiguous,
+ *              16-byte aligned. Rows of h, x_disp, W_* and outputs need a byte
+ *              stride that is a multiple of 16: d and ffn multiples of 8 (bf16)
+ *              or 4 (fp32).
+ *   Ownership  The caller allocates and owns every buffer, the workspace
+ *              included. The library allocates no device memory and keeps no
+ *              per-call state.
+ *   Async      Work is enqueued on `stream`; nothing synchronises. MOE_OK means
+ *              the arguments were valid and every launch was accepted. Failures
+ *              detected on the device (a bounded wait that ran out) are recorded
+ *              in the workspace's status word; read them with moe_read_status.
+ *   Errors     No exceptions cross the ABI. Bad shapes, k < 1, k > N, null
+ *              required pointers or misaligned pointers return
+ *              MOE_ERR_INVALID_ARG before anything is launched. T == 0 returns
+ *              MOE_OK with no launch.
+ *   dtype      MOE_BF16: h, W_*, x_disp, y_rows, y_shared, out are bf16 and the
+ *              GEMMs run on the bf16 tensor cores with fp32 accumulation.
+ *              MOE_F32: the same tensors are fp32 and the GEMMs run as tf32.
+ *              logits and gates are always fp32; indices are int32.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* bad shape, null or misaligned pointer ([P2] sparse_moe raises on bad shapes) */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+  MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 5,       /* device side: a bounded wait ran out (read via moe_read_status) */
+  MOE_ERR_DEVICE_CHECK = 6   /* device side: an index check failed (read via moe_read_status) */
+} moe_status;
+
+typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
+
+/* [P1] §二 第二步 (softmax); [P2] 最常见的 router (sigmoid, as in DeepSeek-V3). */
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score;
+
+/* [P1] §二 第三步 g = p / sum_S p (SELECTED); [P2] Switch top-1 keeps the full
+ * softmax probability, [P3] §2.1 scatters top_probs unrenormalised (NONE). */
+typedef enum { MOE_NORM_SELECTED = 0, MOE_NORM_NONE = 1 } moe_norm;
+
+typedef struct {
+  int64_t T;          /* tokens (flattened batch x sequence, [P1] §三 steps 1-2) */
+  int32_t d;          /* hidden width */
+  int32_t N;          /* routed experts, 1..1024 */
+  int32_t k;          /* experts per token, 1..min(N, 16) */
+  int32_t ffn;        /* routed expert FFN width F */
+  int32_t ffn_shared; /* shared expert FFN width; 0 = no shared expert ([P1] §八) */
+  int32_t dtype;      /* moe_dtype */
+  int32_t score;      /* moe_score */
+  int32_t norm;       /* moe_norm */
+} moe_config;
+
+/* Bytes of device workspace that moe_forward needs for `cfg` (the largest
+ * need of any entry point; every entry point accepts a workspace this size).
+ * Returns 0 for an invalid config. Layout is private to the library. */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* Stage 1+2: router logits, scores, top-k selection and gates.
+ * [P1] §二 第一步-第三步; [P2] 最常见的 router; [P4] first and second steps.
+ *   h          [T, d]  (dtype) hidden states; may be NULL, then logits_in is used
+ *   W_r        [N, d]  (dtype) router weight (rows score one expert each)
+ *   b_r        [N] fp32 or NULL: router bias added to the logits
+ *   sel_bias   [N] fp32 or NULL: per-expert selection bias. It is added to the
+ *              score for SELECTION only; gates use the un-biased scores
+ *              ([P1] §五 auxiliary-loss-free balancing; [P4] bias paragraph)
+ *   logits_in  [T, N] fp32, read iff h == NULL (route given logits, as [P2]
+ *              sparse_moe takes logits)
+ *   logits_out [T, N] fp32 or NULL: the logits z
+ *   idx        [T, k] int32 out: selected experts, by descending selection
+ *              score; equal scores go to the lower expert index first
+ *   gate       [T, k] fp32 out: gate weight of each selected expert
+ */
+moe_status moe_route(const moe_config* cfg, const void* h, const void* W_r,
+                     const float* b_r, const float* sel_bias,
+                     const float* logits_in, float* logits_out,
+                     int32_t* idx, float* gate,
+                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Stage 3+4: regroup (token, slot) pairs by expert and gather their rows.
+ * [P1] §三 Token Dispatch (tokens of one expert listed in ascending order);
+ * [P5] §3 ② Dispatch. Deterministic: rows ordered by (expert, token).
+ *   h          [T, d] (dtype); idx [T, k] int32 from moe_route (each row holds
+ *              k distinct experts in [0, N))
+ *   counts     [N] int32 out: rows per expert
+ *   offsets    [N+1] int32 out: exclusive prefix sum of counts
+ *   row_token  [T*k] int32 out: token of each dispatched row
+ *   inv        [T*k] int32 out: inv[t*k + j] = dispatched row of (t, slot j)
+ *   x_disp     [T*k, d] (dtype) out: x_disp[r] = h[row_token[r]]; may be NULL
+ *              to skip the gather
+ *   ws         scratch for the per-block histograms (see moe_workspace_size)
+ */
+moe_status moe_dispatch(const moe_config* cfg, const void* h, const int32_t* idx,
+                        int32_t* counts, int32_t* offsets, int32_t* row_token,
+                        int32_t* inv, void* x_disp,
+                        void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Stage 5+6: every expert's SwiGLU FFN over its dispatched rows, as one
+ * grouped GEMM pair on the tensor cores (tcgen05, TMA-fed).
+ * [P1] §一 E_i(h) = W_down (SiLU(W_gate h) * W_up h); [P1] §十二 Grouped GEMM;
+ * [P5] §3 ③ and §8 Kernel row.
+ *   x_disp     [T*k, d] (dtype), rows grouped by expert as moe_dispatch writes
+ *   offsets    [N+1] int32 device array from moe_dispatch
+ *   W_gate, W_up [N, ffn, d]; W_down [N, d, ffn] (dtype)
+ *   y_rows     [T*k, d] (dtype) out: y_rows[r] = E_e(x_disp[r]) for row r of expert e
+ *   h, Ws_gate [ffn_shared, d], Ws_up [ffn_shared, d], Ws_down [d, ffn_shared],
+ *   y_shared   [T, d] (dtype) out: the shared expert over all tokens
+ *              ([P1] §八); all five are ignored (may be NULL) when
+ *              cfg->ffn_shared == 0
+ *   ws         holds the [T*k, ffn] (and [T, ffn_shared]) activations
+ */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_disp,
+                          const int32_t* offsets, const void* W_gate,
+                          const void* W_up, const void* W_down, void* y_rows,
+                          const void* h, const void* Ws_gate, const void* Ws_up,
+                          const void* Ws_down, void* y_shared,
+                          void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Stage 7: weighted scatter-ADD of every expert output back to its token.
+ * [P2] 选好以后: outputs are added, never overwritten or concatenated;
+ * [P5] §3 ④ Gather; [P1] §八 shared-expert term.
+ *   out[t] = y_shared[t] + sum_{j<k} gate[t,j] * y_rows[inv[t*k+j]]
+ *   accumulated in fp32 in slot order, stored in dtype.
+ *   y_shared may be NULL (no shared term). out [T, d] (dtype).
+ */
+moe_status moe_combine(const moe_config* cfg, const void* y_rows,
+                       const int32_t* inv, const float* gate,
+                       const void* y_shared, void* out, cudaStream_t stream);
+
+/* The whole layer: route -> dispatch -> grouped SwiGLU (+ shared) -> combine.
+ * [P1] §十四 moe_forward returns (output, logits); [P2] sparse_moe.
+ *   out        [T, d] (dtype) out
+ *   logits_out [T, N] fp32 or NULL
+ *   idx, gate  [T, k] out (as moe_route); counts [N] int32 out or NULL
+ *   Ws_*       NULL when cfg->ffn_shared == 0
+ *   ws         at least moe_workspace_size(cfg) bytes
+ */
+moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r,
+                       const float* b_r, const float* sel_bias,
+                       const void* W_gate, const void* W_up, const void* W_down,
+                       const void* Ws_gate, const void* Ws_up, const void* Ws_down,
+                       void* out, float* logits_out, int32_t* idx, float* gate,
+                       int32_t* counts, void* ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/* Synchronises `stream`, copies the workspace's device status word into
+ * *device_status (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK) and clears
+ * it. Returns MOE_ERR_CUDA if the synchronisation or copy fails. */
+moe_status moe_read_status(void* ws, size_t ws_bytes, int32_t* device_status,
+                           cudaStream_t stream);
+
+/* Test hook for the failure path: launches one CTA that waits on an mbarrier
+ * nothing ever arrives on, for at most `budget_ns` nanoseconds (clamped to
+ * 1 s), then records MOE_ERR_TIMEOUT in the workspace status word and returns.
+ * Never traps and never hangs. */
+moe_status moe_selftest_wait_timeout(uint64_t budget_ns, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream);
+
+/* Human-readable name of a status code. */
+const char* moe_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,168 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
+(stage by stage or as one moe_forward), and compare with the CPU oracle.
+
+Tolerances (derived in the design notes):
+* indices, counts, offsets, permutation: bit-exact; routing decisions within
+  a stated margin of a tie are "ambiguous" and checked for validity instead;
+* gates: 1e-6 absolute against the oracle fed the GPU's own logits;
+* logits: |z_gpu - z| <= d * 2^-24 * sum_i |h_i W_i| + 1e-6 (fp32 summation of
+  exact bf16 products, any order);
+* combine: one rounding to the output dtype: |out - ref| <= 2^-8 |ref| + 1e-6
+  (bf16) or 1e-6 (|ref| + 1) (fp32), ref = the oracle's combine of the GPU's
+  own y_rows and gates;
+* layer output and expert rows: bf16 max-abs <= 2e-2 and rel-L2 <= 5e-3;
+  fp32 (tf32 tensor cores) max-abs <= 1e-2 and rel-L2 <= 2e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import moe_oracle as O
+from top_routing_grouped_bias_b300 import api
+from top_routing_grouped_bias_b300.synth import to_f64
+
+U32 = 2.0 ** -24
+BF16_TOL = dict(max_abs=2e-2, rel_l2=5e-3)
+F32_TOL = dict(max_abs=1e-2, rel_l2=2e-3)
+
+
+def out_tol(w):
+    return F32_TOL if w.dtype == "f32" else BF16_TOL
+
+
+def assert_close_tol(got, ref, tol, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    if got.size == 0:
+        return 0.0, 0.0
+    err = np.abs(got - ref)
+    max_abs = float(err.max())
+    rel_l2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+    assert max_abs <= tol["max_abs"], f"{what}: max-abs {max_abs:.3e} > {tol['max_abs']}"
+    assert rel_l2 <= tol["rel_l2"], f"{what}: rel-L2 {rel_l2:.3e} > {tol['rel_l2']}"
+    return max_abs, rel_l2
+
+
+def np_i(t):
+    return t.detach().cpu().numpy().astype(np.int64)
+
+
+def np_f(t):
+    return to_f64(t)
+
+
+# ------------------------------------------------------------- GPU runs ---
+def gpu_inputs(inp: dict, device="cuda") -> dict:
+    return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def run_staged(cfg, inp: dict, logits_in=None, stream=None) -> dict:
+    """route -> dispatch -> expert FFN -> combine, each through its entry point."""
+    dev = inp["h"].device if inp.get("h") is not None else logits_in.device
+    T, d, N, k, F, Fs = cfg.T, cfg.d, cfg.N, cfg.k, cfg.ffn, cfg.ffn_shared
+    tdt = torch.float32 if cfg.dtype == api.DTYPES["f32"] else torch.bfloat16
+    R = T * k
+    ws = api.alloc_workspace(cfg, dev)
+    r = {}
+    r["logits"] = torch.empty((T, N), dtype=torch.float32, device=dev)
+    r["idx"] = torch.empty((T, k), dtype=torch.int32, device=dev)
+    r["gate"] = torch.empty((T, k), dtype=torch.float32, device=dev)
+    h = inp.get("h") if logits_in is None else None
+    api.moe_route(cfg, h, inp.get("W_r"), inp.get("b_r"), inp.get("sel_bias"), logits_in,
+                  r["logits"], r["idx"], r["gate"], ws, stream)
+    if logits_in is not None:
+        torch.cuda.synchronize()
+        return r
+    r["counts"] = torch.empty((N,), dtype=torch.int32, device=dev)
+    r["offsets"] = torch.empty((N + 1,), dtype=torch.int32, device=dev)
+    r["row_token"] = torch.empty((R,), dtype=torch.int32, device=dev)
+    r["inv"] = torch.empty((T, k), dtype=torch.int32, device=dev)
+    r["x_disp"] = torch.empty((R, d), dtype=tdt, device=dev)
+    api.moe_dispatch(cfg, inp["h"], r["idx"], r["counts"], r["offsets"], r["row_token"], r["inv"],
+                     r["x_disp"], ws, stream)
+    r["y_rows"] = torch.empty((R, d), dtype=tdt, device=dev)
+    r["y_sh"] = torch.empty((T, d), dtype=tdt, device=dev) if Fs > 0 else None
+    api.moe_expert_ffn(cfg, r["x_disp"], r["offsets"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                       r["y_rows"], inp["h"], inp.get("Ws_gate"), inp.get("Ws_up"),
+                       inp.get("Ws_down"), r["y_sh"], ws, stream)
+    r["out"] = torch.empty((T, d), dtype=tdt, device=dev)
+    api.moe_combine(cfg, r["y_rows"], r["inv"], r["gate"], r["y_sh"], r["out"], stream)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    return r
+
+
+def run_forward(cfg, inp: dict, stream=None) -> dict:
+    dev = inp["h"].device
+    tdt = torch.float32 if cfg.dtype == api.DTYPES["f32"] else torch.bfloat16
+    ws = api.alloc_workspace(cfg, dev)
+    outs = api.alloc_outputs(cfg, dev, tdt)
+    api.forward(cfg, inp, outs, ws, stream)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    return dict(outs)
+
+
+# ---------------------------------------------------------- comparisons ---
+def logit_bound(h64, W64):
+    """Per-(token, expert) bound on |z_fp32 - z_exact| for fp32 summation."""
+    d = h64.shape[1]
+    return d * U32 * (np.abs(h64) @ np.abs(W64).T) + 1e-6
+
+
+def selection_scores(z, w_score, bias):
+    p = O.scores(z, w_score)
+    return p if bias is None else p + bias[None, :]
+
+
+def check_selection(idx_gpu, q_ref, k, delta, what=""):
+    """GPU indices vs the oracle's selection on scores q_ref [T,N].
+
+    Tokens whose adjacent gaps among the k+1 best scores are all >= delta
+    must match exactly (set and slot order). Tokens whose set boundary
+    (k-th vs (k+1)-th) gap is >= delta must match as a set. The rest must be a
+    valid choice within delta. Returns the number of ambiguous tokens."""
+    T, N = q_ref.shape
+    S_ref = O.select_topk(q_ref, k)
+    qs = -np.sort(-q_ref, axis=1)
+    top = qs[:, :min(k + 1, N)]
+    gaps = top[:, :-1] - top[:, 1:] if top.shape[1] > 1 else np.full((T, 1), np.inf)
+    order_amb = (gaps[:, :k].min(axis=1) < delta) if gaps.shape[1] else np.zeros(T, bool)
+    set_amb = (gaps[:, k - 1] < delta) if k < N else np.zeros(T, bool)
+    exact = ~order_amb
+    bad = np.nonzero((idx_gpu[exact] != S_ref[exact]).any(axis=1))[0]
+    assert bad.size == 0, f"{what}: {bad.size} tokens differ, e.g. t={np.nonzero(exact)[0][bad[0]]}"
+    for t in np.nonzero(order_amb)[0]:
+        sel = idx_gpu[t]
+        assert len(set(sel.tolist())) == k and (sel >= 0).all() and (sel < N).all()
+        if not set_amb[t]:
+            assert set(sel.tolist()) == set(S_ref[t].tolist()), f"{what}: set differs at t={t}"
+        # each chosen expert is at least as good as the k-th best, up to delta
+        assert (q_ref[t, sel] >= qs[t, k - 1] - delta).all(), f"{what}: invalid choice at t={t}"
+        # slots descend up to delta
+        assert (np.diff(q_ref[t, sel]) <= delta).all(), f"{what}: slot order at t={t}"
+    return int(order_amb.sum())
+
+
+def oracle_gates_from_logits(z_gpu64, idx_gpu, w_score, w_norm):
+    p = O.scores(z_gpu64, w_score)
+    return O.gates_from_scores(p, idx_gpu, w_norm)
+
+
+def check_combine(r, cfg, what="combine"):
+    """GPU out vs the oracle combine of the GPU's own y_rows, inv, gates."""
+    y_rows, inv, g = np_f(r["y_rows"]), np_i(r["inv"]), np_f(r["gate"])
+    ysh = None if r.get("y_sh") is None else np_f(r["y_sh"])
+    ref = O.combine(y_rows, inv, g, ysh)
+    got = np_f(r["out"])
+    # fp32 accumulation error E (k+1 fused steps), then one rounding to dtype
+    mag = O.combine(np.abs(y_rows), inv, np.abs(g), None if ysh is None else np.abs(ysh))
+    E = (inv.shape[1] + 1) * U32 * mag + 1e-30
+    if cfg.dtype == api.DTYPES["f32"]:
+        bound = U32 * 2 * (np.abs(ref) + E) + E
+    else:
+        bound = 2.0 ** -8 * (np.abs(ref) + E) + E
+    viol = np.abs(got - ref) > bound
+    assert not viol.any(), f"{what}: {int(viol.sum())} elements beyond one rounding"

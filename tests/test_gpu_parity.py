@@ -1,0 +1,293 @@
+"""GPU parity of every stage and of the whole layer against the CPU oracle, on
+small seeded workloads that span several tiles and ragged tails, plus the
+pages' worked examples run through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import load_golden
+from gpu_helpers import (BF16_TOL, F32_TOL, assert_close_tol, check_combine, check_selection,
+                         gpu_inputs, logit_bound, np_f, np_i, oracle_gates_from_logits,
+                         out_tol, run_forward, run_staged, selection_scores)
+from oracle import moe_oracle as O
+from top_routing_grouped_bias_b300 import api, synth
+from top_routing_grouped_bias_b300.synth import Workload, to_f64
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    # 300 tokens over 8 experts: ragged last m-tile per expert, 3 gate/up n-tiles
+    "ragged_softmax_top2": Workload("ragged_softmax_top2", T=300, d=256, N=8, F=384, k=2),
+    # ~500 rows per expert (4 m-tiles), ragged n-tile (F=320), K tails, d=192 < down tile
+    "multi_mtile_ragged_n": Workload("multi_mtile_ragged_n", T=1000, d=192, N=4, F=320, k=2),
+    # sigmoid + Zipf selection bias + shared expert; several experts get no rows
+    "sigmoid_bias_shared": Workload("sigmoid_bias_shared", T=257, d=128, N=16, F=128, k=4,
+                                    F_sh=256, score="sigmoid", bias_zipf_s=1.1),
+    # Switch style: full softmax, top-1, no renormalisation
+    "switch_top1": Workload("switch_top1", T=513, d=128, N=8, F=192, k=1, norm="none"),
+    # the tiny fp32 workload (tf32 tensor cores)
+    "tiny_fp32": synth.WORKLOADS["tiny_fp32"],
+    "tiny_fp32_shared": synth.WORKLOADS["tiny_fp32"].replace(name="tiny_fp32_shared", F_sh=128,
+                                                             score="sigmoid", bias_zipf_s=1.1),
+    "single_token": Workload("single_token", T=1, d=64, N=4, F=64, k=2),
+    "one_expert": Workload("one_expert", T=130, d=64, N=1, F=128, k=1),
+    "k_equals_N": Workload("k_equals_N", T=64, d=64, N=4, F=64, k=4),
+    # more experts than tokens can cover: many empty groups, N > 256
+    "many_experts": Workload("many_experts", T=200, d=64, N=300, F=64, k=8, score="sigmoid",
+                             bias_zipf_s=1.1),
+    "softmax_bias_none": Workload("softmax_bias_none", T=333, d=128, N=32, F=128, k=3,
+                                  norm="none", bias_zipf_s=1.1, bias_beta=0.05),
+}
+
+
+def oracle_inputs(inp):
+    return {k: to_f64(v) for k, v in inp.items()}
+
+
+def reference_layer(w, o, idx_gpu):
+    """Oracle layer output in fp64 with the GPU's (validated) selection:
+    gates from the oracle's own fp64 logits, experts and combine in fp64."""
+    z = O.router_logits(o["h"], o["W_r"])
+    p = O.scores(z, w.score)
+    g = O.gates_from_scores(p, idx_gpu, w.norm)
+    counts, offsets, row_token, inv = O.dispatch(idx_gpu, w.N)
+    y_rows = O.expert_rows(o["h"][row_token], offsets, o["W_gate"], o["W_up"], o["W_down"])
+    ysh = None
+    if w.F_sh > 0:
+        ysh = O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"])
+    return O.combine(y_rows, inv, g, ysh), y_rows, ysh
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_workload_stagewise_parity(cuda_lib, name):
+    w = SMALL[name]
+    cfg = api.config_for(w)
+    inp = synth.make_inputs(w, seed=0, device="cpu")
+    o = oracle_inputs(inp)
+    r = run_staged(cfg, gpu_inputs(inp))
+
+    # ---- logits ----
+    z_ref = O.router_logits(o["h"], o["W_r"])
+    z_gpu = np_f(r["logits"])
+    bound = logit_bound(o["h"], o["W_r"])
+    assert (np.abs(z_gpu - z_ref) <= bound).all(), "logits beyond the fp32 summation bound"
+
+    # ---- selection: given the GPU logits (decision precision of the kernel) ----
+    idx = np_i(r["idx"])
+    q_given = selection_scores(z_gpu, w.score, o["sel_bias"])
+    delta_given = 0.0 if o["sel_bias"] is None else 4e-6
+    check_selection(idx, q_given, w.k, delta_given, f"{name} given logits")
+    # ---- selection end to end: ambiguous within the logit error ----
+    q_ref = selection_scores(z_ref, w.score, o["sel_bias"])
+    dz = float(bound.max())
+    delta = 4 * dz + (4e-6 if o["sel_bias"] is not None else 0.0)
+    n_amb = check_selection(idx, q_ref, w.k, delta, f"{name} end to end")
+    assert n_amb <= max(2, w.T // 50), n_amb
+
+    # ---- gates: oracle fed the GPU's logits and indices ----
+    g_ref = oracle_gates_from_logits(z_gpu, idx, w.score, w.norm)
+    np.testing.assert_allclose(np_f(r["gate"]), g_ref, atol=1e-6, rtol=0)
+
+    # ---- dispatch: bit-exact given the GPU's indices ----
+    counts, offsets, row_token, inv = O.dispatch(idx, w.N)
+    assert np_i(r["counts"]).tolist() == counts.tolist()
+    assert np_i(r["offsets"]).tolist() == offsets.tolist()
+    assert np_i(r["row_token"]).tolist() == row_token.tolist()
+    assert (np_i(r["inv"]) == inv).all()
+    assert torch.equal(r["x_disp"].cpu(), inp["h"][torch.from_numpy(row_token)])
+
+    # ---- expert rows and shared expert ----
+    y_ref = O.expert_rows(o["h"][row_token], offsets, o["W_gate"], o["W_up"], o["W_down"])
+    assert_close_tol(np_f(r["y_rows"]), y_ref, out_tol(w), f"{name} y_rows")
+    if w.F_sh > 0:
+        ysh_ref = O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"])
+        assert_close_tol(np_f(r["y_sh"]), ysh_ref, out_tol(w), f"{name} y_shared")
+
+    # ---- combine: one rounding of the GPU's own terms ----
+    check_combine(r, cfg, f"{name} combine")
+
+    # ---- whole layer ----
+    out_ref, _, _ = reference_layer(w, o, idx)
+    assert_close_tol(np_f(r["out"]), out_ref, out_tol(w), f"{name} out")
+
+
+@pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "tiny_fp32",
+                                  "many_experts"])
+def test_forward_equals_stages_and_is_deterministic(cuda_lib, name):
+    w = SMALL[name]
+    cfg = api.config_for(w)
+    inp = gpu_inputs(synth.make_inputs(w, seed=3, device="cpu"))
+    a = run_forward(cfg, inp)
+    b = run_forward(cfg, inp)
+    s = run_staged(cfg, inp)
+    for key in ("out", "idx", "gate", "logits", "counts"):
+        assert torch.equal(a[key], b[key]), f"{key} not deterministic"
+        assert torch.equal(a[key], s[key]), f"{key}: forward differs from the stages"
+
+
+def test_forward_matches_dense_masked_oracle(cuda_lib):
+    """The layer output equals the pages' dense masked computation."""
+    w = Workload("dense_check", T=96, d=64, N=6, F=64, k=2, F_sh=64)
+    cfg = api.config_for(w)
+    inp = synth.make_inputs(w, seed=5, device="cpu")
+    o = oracle_inputs(inp)
+    r = run_forward(cfg, gpu_inputs(inp))
+    y_dense, z, S, g = O.moe_forward_dense(o["h"], o["W_r"], o["W_gate"], o["W_up"], o["W_down"],
+                                           w.k, shared=(o["Ws_gate"], o["Ws_up"], o["Ws_down"]))
+    n_amb = check_selection(np_i(r["idx"]), O.softmax(z), w.k, 1e-4, "dense")
+    assert n_amb == 0
+    assert_close_tol(np_f(r["out"]), y_dense, BF16_TOL, "dense masked")
+
+
+# ---------------------------------------------------- route from logits ---
+def _route_given(cfg, z, bias=None):
+    dev = "cuda"
+    inp = {"h": None, "W_r": None, "sel_bias": None if bias is None else bias.to(dev)}
+    return run_staged(cfg, inp, logits_in=z.to(dev))
+
+
+def test_route_page1_example(cuda_lib):
+    g = load_golden("page1_softmax_example.json")
+    z = torch.tensor([g["logits"]], dtype=torch.float32)
+    cfg = api.make_config(1, 8, 4, g["k"], 8)
+    r = _route_given(cfg, z)
+    assert np_i(r["idx"])[0].tolist() == g["selected"]
+    np.testing.assert_allclose(np_f(r["gate"])[0], g["gates_printed"], atol=g["printed_abs_tol"])
+    np.testing.assert_allclose(np_f(r["gate"]), O.gates_from_selected_logits(
+        to_f64(z), np_i(r["idx"])), atol=1e-6)
+
+
+def test_route_page2_example_and_switch(cuda_lib):
+    g = load_golden("page2_selected_renorm_example.json")
+    z = torch.tensor([g["scores"]], dtype=torch.float32)
+    r = _route_given(api.make_config(1, 8, 3, 2, 8), z)
+    assert np_i(r["idx"])[0].tolist() == g["selected"]
+    np.testing.assert_allclose(np_f(r["gate"])[0], g["gates_printed"], atol=g["printed_abs_tol"])
+    # Switch: top-1 keeps the full softmax probability
+    r1 = _route_given(api.make_config(1, 8, 3, 1, 8, norm="none"), z)
+    np.testing.assert_allclose(np_f(r1["gate"])[0, 0], O.softmax(to_f64(z))[0, 0], atol=1e-6)
+
+
+@pytest.mark.parametrize("N,k", [(5, 2), (33, 1), (64, 8), (300, 16), (1024, 4), (7, 7)])
+@pytest.mark.parametrize("score", ["softmax", "sigmoid"])
+@pytest.mark.parametrize("norm", ["selected", "none"])
+def test_route_given_logits_ties_exact(cuda_lib, N, k, score, norm):
+    """Logits on a coarse grid (many exact ties): indices must equal the
+    oracle's lowest-index tie-break exactly; gates within 1e-6."""
+    T = 777
+    z = synth.random_logits(T, N, seed=N * 31 + k, std=1.5, ties=True)
+    cfg = api.make_config(T, 8, N, k, 8, score=score, norm=norm)
+    r = _route_given(cfg, z)
+    z64 = to_f64(z)
+    S, g, _, _ = O.route(z64, k, score, norm)
+    assert (np_i(r["idx"]) == S).all()
+    np.testing.assert_allclose(np_f(r["gate"]), g, atol=1e-6, rtol=0)
+    np.testing.assert_array_equal(np_f(r["logits"]), z64)
+
+
+@pytest.mark.parametrize("score", ["softmax", "sigmoid"])
+def test_route_given_logits_with_bias(cuda_lib, score):
+    T, N, k = 1000, 64, 6
+    z = synth.random_logits(T, N, seed=11, std=1.0)
+    bias = synth.zipf_bias(torch.Generator().manual_seed(2), N, 1.1, 0.3, "cpu")
+    r = _route_given(api.make_config(T, 8, N, k, 8, score=score), z, bias)
+    z64 = to_f64(z)
+    q = selection_scores(z64, score, to_f64(bias))
+    check_selection(np_i(r["idx"]), q, k, 4e-6, "bias given logits")
+    g_ref = oracle_gates_from_logits(z64, np_i(r["idx"]), score, "selected")
+    np.testing.assert_allclose(np_f(r["gate"]), g_ref, atol=1e-6, rtol=0)
+
+
+# -------------------------------------------------------------- dispatch ---
+def _dispatch(cfg, idx, h):
+    dev = "cuda"
+    R = cfg.T * cfg.k
+    ws = api.alloc_workspace(cfg, dev)
+    out = dict(counts=torch.empty(cfg.N, dtype=torch.int32, device=dev),
+               offsets=torch.empty(cfg.N + 1, dtype=torch.int32, device=dev),
+               row_token=torch.empty(R, dtype=torch.int32, device=dev),
+               inv=torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev),
+               x_disp=torch.empty((R, cfg.d), dtype=h.dtype, device=dev))
+    api.moe_dispatch(cfg, h.to(dev), idx.to(dev), out["counts"], out["offsets"], out["row_token"],
+                     out["inv"], out["x_disp"], ws)
+    torch.cuda.synchronize()
+    return out
+
+
+def test_dispatch_page1_table(cuda_lib):
+    gd = load_golden("page1_dispatch_table.json")
+    idx = torch.tensor([[e for e, _ in row] for row in gd["choices"]], dtype=torch.int32)
+    h = torch.arange(4 * 8, dtype=torch.float32).reshape(4, 8).to(torch.bfloat16)
+    r = _dispatch(api.make_config(4, 8, gd["N"], 2, 8), idx, h)
+    assert np_i(r["counts"]).tolist() == gd["counts"]
+    assert np_i(r["offsets"]).tolist() == gd["offsets"]
+    rt = np_i(r["row_token"])
+    for e, toks in gd["buckets"].items():
+        e = int(e)
+        assert rt[gd["offsets"][e]:gd["offsets"][e + 1]].tolist() == toks
+    assert torch.equal(r["x_disp"].cpu(), h[torch.from_numpy(rt)])
+
+
+@pytest.mark.parametrize("T,N,k", [(1, 1, 1), (255, 7, 3), (256, 128, 1), (257, 16, 16),
+                                   (5000, 1024, 4), (4099, 3, 2)])
+def test_dispatch_random_exact(cuda_lib, T, N, k):
+    gen = torch.Generator().manual_seed(T + N + k)
+    idx = torch.stack([torch.randperm(N, generator=gen)[:k] for _ in range(T)]).to(torch.int32)
+    d = 24
+    h = torch.randn((T, d), generator=gen).to(torch.bfloat16)
+    r = _dispatch(api.make_config(T, d, N, k, 8), idx, h)
+    counts, offsets, row_token, inv = O.dispatch(idx.numpy(), N)
+    assert np_i(r["counts"]).tolist() == counts.tolist()
+    assert np_i(r["offsets"]).tolist() == offsets.tolist()
+    assert np_i(r["row_token"]).tolist() == row_token.tolist()
+    assert (np_i(r["inv"]) == inv).all()
+    assert torch.equal(r["x_disp"].cpu(), h[torch.from_numpy(row_token)])
+
+
+# --------------------------------------------------------------- combine ---
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_combine_page2_example(cuda_lib, dtype):
+    gd = load_golden("page2_combine_example.json")
+    S = np.array([[e for e, _ in row] for row in gd["choices"]])
+    g = np.array([[w for _, w in row] for row in gd["choices"]])
+    counts, offsets, row_token, inv = O.dispatch(S, gd["N"])
+    d = 8                                          # the 2-wide example padded to 8
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    y_rows = torch.zeros((4, d), dtype=tdt)
+    for t in range(2):
+        for j in range(2):
+            y_rows[inv[t, j], :2] = torch.tensor(gd["expert_outputs"][f"{t}:{S[t, j]}"])
+    cfg = api.make_config(2, d, gd["N"], 2, 8, dtype=dtype)
+    out = torch.empty((2, d), dtype=tdt, device="cuda")
+    api.moe_combine(cfg, y_rows.cuda(), torch.from_numpy(inv).to(torch.int32).cuda(),
+                    torch.from_numpy(g).to(torch.float32).cuda(), None, out)
+    torch.cuda.synchronize()
+    got = np_f(out)
+    tol = 1e-6 if dtype == "f32" else 2.0 ** -8 * 2.6
+    np.testing.assert_allclose(got[:, :2], gd["y_printed"], atol=tol, rtol=0)
+    assert (got[:, 2:] == 0).all()
+
+
+# ------------------------------------------------------------ expert FFN ---
+def test_single_expert_is_dense_swiglu_vs_library(cuda_lib):
+    """N=1, k=1: the grouped GEMM pair is a plain SwiGLU FFN; check against
+    torch.matmul + F.silu in fp32 on the same bf16 values."""
+    w = Workload("dense1", T=1000, d=512, N=1, F=768, k=1)
+    cfg = api.config_for(w)
+    inp = gpu_inputs(synth.make_inputs(w, seed=9, device="cpu"))
+    r = run_staged(cfg, inp)
+    h = inp["h"].float()
+    act = torch.nn.functional.silu(h @ inp["W_gate"][0].float().T) * (h @ inp["W_up"][0].float().T)
+    ref = act.to(torch.bfloat16).float() @ inp["W_down"][0].float().T
+    assert_close_tol(np_f(r["y_rows"]), to_f64(ref), BF16_TOL, "dense SwiGLU vs library")
+
+
+def test_zero_weight_routed_experts_leave_shared_only(cuda_lib):
+    w = Workload("shared_only", T=200, d=128, N=8, F=128, k=2, F_sh=256)
+    cfg = api.config_for(w)
+    inp = synth.make_inputs(w, seed=4, device="cpu")
+    inp["W_down"] = torch.zeros_like(inp["W_down"])
+    o = oracle_inputs(inp)
+    r = run_forward(cfg, gpu_inputs(inp))
+    ref = O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"])
+    assert_close_tol(np_f(r["out"]), ref, BF16_TOL, "shared only")

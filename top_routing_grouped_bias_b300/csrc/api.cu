@@ -1,0 +1,230 @@
+// Host side of the C ABI declared in include/moe.h: argument validation,
+// workspace carving and the launch sequence of each entry point.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "internal.h"
+
+using namespace moe;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Pure host checks of a config; no CUDA calls.
+moe_status check_config(const moe_config* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->T > (int64_t(1) << 31) / 16) return MOE_ERR_INVALID_ARG;
+  if (c->d < 1 || c->N < 1 || c->N > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (c->k < 1 || c->k > c->N || c->k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+  if (c->ffn < 1 || c->ffn_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_BF16 && c->dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c->norm != MOE_NORM_SELECTED && c->norm != MOE_NORM_NONE) return MOE_ERR_INVALID_ARG;
+  const int vec = c->dtype == MOE_F32 ? 4 : 8;  // elements per 16 bytes
+  if (c->d % vec != 0 || c->ffn % vec != 0 || c->ffn_shared % vec != 0) return MOE_ERR_INVALID_ARG;
+  // dispatched rows and B-operand rows must index with int32 on the device
+  const int64_t R = c->T * c->k;
+  if (R * int64_t(c->d) >= (int64_t(1) << 40)) return MOE_ERR_INVALID_ARG;
+  if (int64_t(c->N) * c->ffn >= (int64_t(1) << 31) || int64_t(c->N) * c->d >= (int64_t(1) << 31))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+bool ok_tensor(const void* p) { return p != nullptr && aligned(p, 16); }
+bool ok_f32(const void* p) { return p != nullptr && aligned(p, 4); }
+bool ok_opt_f32(const void* p) { return p == nullptr || aligned(p, 4); }
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off);
+}
+
+moe_status route_impl(const moe_config* cfg, const void* h, const void* W_r, const float* b_r,
+                      const float* sel_bias, const float* logits_in, float* logits_out,
+                      int32_t* idx, float* gate, cudaStream_t stream) {
+  if (h != nullptr) {
+    if (!ok_tensor(h) || !ok_tensor(W_r)) return MOE_ERR_INVALID_ARG;
+  } else if (!ok_f32(logits_in)) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!ok_f32(idx) || !ok_f32(gate) || !ok_opt_f32(b_r) || !ok_opt_f32(sel_bias) ||
+      !ok_opt_f32(logits_out))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  RouteArgs a{};
+  a.h = h; a.W_r = W_r; a.b_r = b_r; a.sel_bias = sel_bias; a.logits_in = logits_in;
+  a.logits_out = logits_out; a.idx = idx; a.gate = gate; a.T = cfg->T; a.d = cfg->d;
+  a.N = cfg->N; a.k = cfg->k; a.score = cfg->score; a.norm = cfg->norm; a.dtype = cfg->dtype;
+  return from_cuda(launch_route(a, stream));
+}
+
+moe_status dispatch_impl(const moe_config* cfg, const void* h, const int32_t* idx, int32_t* counts,
+                         int32_t* offsets, int32_t* row_token, int32_t* inv, void* x_disp,
+                         void* ws, const WsLayout& L, cudaStream_t stream) {
+  if (!ok_f32(idx) || !ok_f32(counts) || !ok_f32(offsets) || !ok_f32(row_token) || !ok_f32(inv))
+    return MOE_ERR_INVALID_ARG;
+  if (x_disp != nullptr && (!ok_tensor(x_disp) || !ok_tensor(h))) return MOE_ERR_INVALID_ARG;
+  DispatchArgs a{};
+  a.h = h; a.idx = idx; a.counts = counts; a.offsets = offsets; a.row_token = row_token;
+  a.inv = inv; a.x_disp = x_disp; a.block_base = at<int32_t>(ws, L.block_base);
+  a.status = at<int32_t>(ws, L.status);
+  a.T = cfg->T; a.d = cfg->d; a.N = cfg->N; a.k = cfg->k; a.dtype = cfg->dtype;
+  return from_cuda(launch_dispatch(a, stream));
+}
+
+moe_status ffn_impl(const moe_config* cfg, const void* x_disp, const int32_t* offsets,
+                    const void* W_gate, const void* W_up, const void* W_down, void* y_rows,
+                    const void* h, const void* Ws_gate, const void* Ws_up, const void* Ws_down,
+                    void* y_shared, void* ws, const WsLayout& L, cudaStream_t stream) {
+  if (!ok_tensor(x_disp) || !ok_f32(offsets) || !ok_tensor(W_gate) || !ok_tensor(W_up) ||
+      !ok_tensor(W_down) || !ok_tensor(y_rows))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->ffn_shared > 0 && (!ok_tensor(h) || !ok_tensor(Ws_gate) || !ok_tensor(Ws_up) ||
+                              !ok_tensor(Ws_down) || !ok_tensor(y_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  FfnArgs a{};
+  a.x_disp = x_disp; a.offsets = offsets; a.W_gate = W_gate; a.W_up = W_up; a.W_down = W_down;
+  a.y_rows = y_rows; a.h = h; a.Ws_gate = Ws_gate; a.Ws_up = Ws_up; a.Ws_down = Ws_down;
+  a.y_shared = y_shared; a.act = at<void>(ws, L.act); a.act_sh = at<void>(ws, L.act_sh);
+  a.status = at<int32_t>(ws, L.status);
+  a.T = cfg->T; a.d = cfg->d; a.N = cfg->N; a.k = cfg->k; a.F = cfg->ffn; a.F_sh = cfg->ffn_shared;
+  a.dtype = cfg->dtype;
+  return from_cuda(launch_expert_ffn(a, stream));
+}
+
+moe_status combine_impl(const moe_config* cfg, const void* y_rows, const int32_t* inv,
+                        const float* gate, const void* y_shared, void* out, cudaStream_t stream) {
+  if (!ok_tensor(y_rows) || !ok_f32(inv) || !ok_f32(gate) || !ok_tensor(out))
+    return MOE_ERR_INVALID_ARG;
+  if (y_shared != nullptr && !ok_tensor(y_shared)) return MOE_ERR_INVALID_ARG;
+  CombineArgs a{};
+  a.y_rows = y_rows; a.inv = inv; a.gate = gate; a.y_shared = y_shared; a.out = out;
+  a.T = cfg->T; a.d = cfg->d; a.k = cfg->k; a.dtype = cfg->dtype;
+  return from_cuda(launch_combine(a, stream));
+}
+
+bool ws_ok(void* ws, size_t ws_bytes, size_t need) {
+  return ws != nullptr && aligned(ws, 256) && ws_bytes >= need;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_config* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  return ws_layout(*cfg).total;
+}
+
+moe_status moe_route(const moe_config* cfg, const void* h, const void* W_r, const float* b_r,
+                     const float* sel_bias, const float* logits_in, float* logits_out,
+                     int32_t* idx, float* gate, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  return route_impl(cfg, h, W_r, b_r, sel_bias, logits_in, logits_out, idx, gate, stream);
+}
+
+moe_status moe_dispatch(const moe_config* cfg, const void* h, const int32_t* idx, int32_t* counts,
+                        int32_t* offsets, int32_t* row_token, int32_t* inv, void* x_disp, void* ws,
+                        size_t ws_bytes, cudaStream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  const WsLayout L = ws_layout(*cfg);
+  if (!ws_ok(ws, ws_bytes, L.end_dispatch)) return MOE_ERR_WORKSPACE;
+  return dispatch_impl(cfg, h, idx, counts, offsets, row_token, inv, x_disp, ws, L, stream);
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_disp, const int32_t* offsets,
+                          const void* W_gate, const void* W_up, const void* W_down, void* y_rows,
+                          const void* h, const void* Ws_gate, const void* Ws_up,
+                          const void* Ws_down, void* y_shared, void* ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  const WsLayout L = ws_layout(*cfg);
+  if (!ws_ok(ws, ws_bytes, L.end_ffn)) return MOE_ERR_WORKSPACE;
+  return ffn_impl(cfg, x_disp, offsets, W_gate, W_up, W_down, y_rows, h, Ws_gate, Ws_up, Ws_down,
+                  y_shared, ws, L, stream);
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* y_rows, const int32_t* inv,
+                       const float* gate, const void* y_shared, void* out, cudaStream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->T == 0) return MOE_OK;
+  return combine_impl(cfg, y_rows, inv, gate, y_shared, out, stream);
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r, const float* b_r,
+                       const float* sel_bias, const void* W_gate, const void* W_up,
+                       const void* W_down, const void* Ws_gate, const void* Ws_up,
+                       const void* Ws_down, void* out, float* logits_out, int32_t* idx,
+                       float* gate, int32_t* counts, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!ok_tensor(h) || !ok_tensor(W_r) || !ok_tensor(W_gate) || !ok_tensor(W_up) ||
+      !ok_tensor(W_down) || !ok_tensor(out) || !ok_f32(idx) || !ok_f32(gate) ||
+      !ok_opt_f32(counts) || !ok_opt_f32(logits_out))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->ffn_shared > 0 && (!ok_tensor(Ws_gate) || !ok_tensor(Ws_up) || !ok_tensor(Ws_down)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  if (!ws_ok(ws, ws_bytes, L.total)) return MOE_ERR_WORKSPACE;
+  if (cfg->T == 0) return MOE_OK;
+  int32_t* cnt = counts != nullptr ? counts : at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* row_token = at<int32_t>(ws, L.row_token);
+  int32_t* inv = at<int32_t>(ws, L.inv);
+  void* x_disp = at<void>(ws, L.x_disp);
+  void* y_rows = at<void>(ws, L.y_rows);
+  void* y_sh = cfg->ffn_shared > 0 ? at<void>(ws, L.y_sh) : nullptr;
+
+  s = route_impl(cfg, h, W_r, b_r, sel_bias, nullptr, logits_out, idx, gate, stream);
+  if (s != MOE_OK) return s;
+  s = dispatch_impl(cfg, h, idx, cnt, offsets, row_token, inv, x_disp, ws, L, stream);
+  if (s != MOE_OK) return s;
+  s = ffn_impl(cfg, x_disp, offsets, W_gate, W_up, W_down, y_rows, h, Ws_gate, Ws_up, Ws_down,
+               y_sh, ws, L, stream);
+  if (s != MOE_OK) return s;
+  return combine_impl(cfg, y_rows, inv, gate, y_sh, out, stream);
+}
+
+moe_status moe_read_status(void* ws, size_t ws_bytes, int32_t* device_status, cudaStream_t stream) {
+  if (ws == nullptr || ws_bytes < 256 || device_status == nullptr) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
+  *device_status = v;
+  return MOE_OK;
+}
+
+moe_status moe_selftest_wait_timeout(uint64_t budget_ns, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+  if (ws == nullptr || ws_bytes < 256 || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  if (budget_ns > 1000000000ull) budget_ns = 1000000000ull;
+  return from_cuda(launch_selftest_wait(static_cast<int32_t*>(ws), budget_ns, stream));
+}
+
+const char* moe_status_string(int32_t status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+    default: return "MOE_UNKNOWN_STATUS";
+  }
+}
+
+}  // extern "C"

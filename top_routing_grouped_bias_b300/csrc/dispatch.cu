@@ -1,0 +1,199 @@
+// Dispatch: regroup the (token, slot) pairs by expert and gather their rows.
+//
+// Pages: "MOE 专家选择与路由机制" §三 Token Dispatch (pairs of one expert are
+// listed together, tokens ascending); "【大模型】MoE（专家混合模型）简介" §3 ②.
+//
+// Deterministic counting sort in three launches, no atomics on the ordering:
+//   1. count    per block of 256 tokens, per-expert pair counts -> base[b][e]
+//   2. scan     counts[e] = sum_b, offsets = exclusive scan over e, and
+//               base[b][e] = offsets[e] + sum_{b' < b} count[b'][e]
+//   3. permute  per block: per-warp counts, scan over warps, then the rank of
+//               each pair among earlier pairs of the same expert in its warp;
+//               row = base + warp prefix + rank. Writes row_token, inv and
+//               copies h[t] into its k dispatched rows (16-byte vectors).
+// The row of (t, e) is offsets[e] + #{t' < t : e in S_t'}, i.e. rows are
+// ordered by (expert, token).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTB = kDispatchTokensPerBlock;  // 256 tokens, 8 warps
+constexpr int kWarps = kTB / 32;
+
+__global__ void __launch_bounds__(kTB) dispatch_count_kernel(DispatchArgs a) {
+  extern __shared__ int hist[];  // [N]
+  for (int e = threadIdx.x; e < a.N; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kTB + threadIdx.x;
+  if (t < a.T) {
+    for (int j = 0; j < a.k; ++j) {
+      const int e = a.idx[t * a.k + j];
+      if (e >= 0 && e < a.N)
+        atomicAdd(&hist[e], 1);
+      else
+        atomicCAS(a.status, 0, MOE_ERR_DEVICE_CHECK);
+    }
+  }
+  __syncthreads();
+  int32_t* base = a.block_base + static_cast<size_t>(blockIdx.x) * a.N;
+  for (int e = threadIdx.x; e < a.N; e += blockDim.x) base[e] = hist[e];
+}
+
+// One block of 1024 threads.
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(DispatchArgs a, int nb) {
+  __shared__ int tot[kMaxExperts];
+  __shared__ int warp_sums[32];
+  const int N = a.N;
+  // per-expert running sum over blocks (exclusive), column by column
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nb; ++b) {
+      int32_t* p = a.block_base + static_cast<size_t>(b) * N + e;
+      const int c = *p;
+      *p = run;
+      run += c;
+    }
+    tot[e] = run;
+  }
+  __syncthreads();
+  // exclusive scan of tot[0..N) with one block: each thread owns a contiguous chunk
+  const int per = (N + blockDim.x - 1) / blockDim.x;
+  const int lo = threadIdx.x * per, hi = min(N, lo + per);
+  int local = 0;
+  for (int e = lo; e < hi; ++e) local += tot[e];
+  // block exclusive scan of `local`
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int v = lane < (blockDim.x >> 5) ? warp_sums[lane] : 0;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
+    }
+    warp_sums[lane] = inc - v;  // exclusive prefix of warps
+  }
+  __syncthreads();
+  int run = warp_sums[w] + incl - local;
+  for (int e = lo; e < hi; ++e) {
+    a.counts[e] = tot[e];
+    a.offsets[e] = run;
+    run += tot[e];
+  }
+  if (hi == N && lo < hi) a.offsets[N] = run;  // the owner of expert N-1 (N >= 1)
+  __syncthreads();
+  // add the expert offsets to every block's base
+  for (int b = 0; b < nb; ++b) {
+    int32_t* p = a.block_base + static_cast<size_t>(b) * N;
+    for (int e = threadIdx.x; e < N; e += blockDim.x) p[e] += a.offsets[e];
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
+  extern __shared__ int sm[];
+  const int N = a.N, k = a.k;
+  int* whist = sm;                                   // [kWarps][N]
+  int* sidx = sm + kWarps * N;                       // [kWarps][32][k]
+  int* srow = sidx + kWarps * 32 * k;                // [kWarps][32][k]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kWarps * N; i += blockDim.x) whist[i] = 0;
+  __syncthreads();
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kTB + threadIdx.x;
+  const bool valid = t < a.T;
+  int* my_idx = sidx + (warp * 32 + lane) * k;
+  for (int j = 0; j < k; ++j) {
+    int e = valid ? a.idx[t * k + j] : -1;
+    if (e < 0 || e >= N) e = -1;  // out-of-range indices were flagged by the count pass
+    my_idx[j] = e;
+    if (e >= 0) atomicAdd(&whist[warp * N + e], 1);
+  }
+  __syncthreads();
+  // per expert: exclusive scan over warps, plus the block base
+  const int32_t* base = a.block_base + static_cast<size_t>(blockIdx.x) * N;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    int run = base[e];
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = whist[w * N + e];
+      whist[w * N + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  if (valid) {
+    const int* wid = sidx + warp * 32 * k;
+    for (int j = 0; j < k; ++j) {
+      const int e = my_idx[j];
+      if (e < 0) {
+        a.inv[t * k + j] = -1;
+        srow[(warp * 32 + lane) * k + j] = -1;
+        continue;
+      }
+      int rank = 0;
+      for (int l = 0; l < lane; ++l)
+        for (int jj = 0; jj < k; ++jj) rank += (wid[l * k + jj] == e);
+      const int row = whist[warp * N + e] + rank;
+      a.row_token[row] = static_cast<int32_t>(t);
+      a.inv[t * k + j] = row;
+      srow[(warp * 32 + lane) * k + j] = row;
+    }
+  }
+  __syncwarp();
+  if (a.x_disp == nullptr) return;
+  // gather: each warp copies its 32 tokens' rows into their k dispatched rows
+  const int nvec = a.d * static_cast<int>(sizeof(T)) / 16;
+  const uint4* H = static_cast<const uint4*>(a.h);
+  uint4* X = static_cast<uint4*>(a.x_disp);
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTB + warp * 32;
+  for (int l = 0; l < 32; ++l) {
+    const int64_t tt = t0 + l;
+    if (tt >= a.T) break;
+    const int* rows = srow + (warp * 32 + l) * k;
+    const uint4* src = H + tt * nvec;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 val = src[v];
+      for (int j = 0; j < k; ++j)
+        if (rows[j] >= 0) X[static_cast<int64_t>(rows[j]) * nvec + v] = val;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
+  if (a.T == 0) {
+    cudaError_t e1 = cudaMemsetAsync(a.counts, 0, sizeof(int32_t) * a.N, stream);
+    if (e1 != cudaSuccess) return e1;
+    return cudaMemsetAsync(a.offsets, 0, sizeof(int32_t) * (a.N + 1), stream);
+  }
+  const int nb = static_cast<int>((a.T + kTB - 1) / kTB);
+  dispatch_count_kernel<<<nb, kTB, a.N * sizeof(int), stream>>>(a);
+  dispatch_scan_kernel<<<1, 1024, 0, stream>>>(a, nb);
+  const size_t smem = sizeof(int) * (static_cast<size_t>(kWarps) * a.N + 2u * kWarps * 32 * a.k);
+  cudaError_t err;
+  if (a.dtype == MOE_F32) {
+    err = cudaFuncSetAttribute(dispatch_permute_kernel<float>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    dispatch_permute_kernel<float><<<nb, kTB, smem, stream>>>(a);
+  } else {
+    err = cudaFuncSetAttribute(dispatch_permute_kernel<__nv_bfloat16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    dispatch_permute_kernel<__nv_bfloat16><<<nb, kTB, smem, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,556 @@
+// Grouped GEMM for the expert FFNs on the 5th-generation tensor cores.
+//
+// Pages: "MOE 专家选择与路由机制" §一 (E_i(h) = W_down (SiLU(W_gate h) ⊙ W_up h))
+// and §十二 (Grouped GEMM for many small per-expert matrices);
+// "【大模型】MoE（专家混合模型）简介" §3 ③ and §8 (Grouped GEMM kernel).
+//
+// One persistent launch per pass runs every expert's rows (a "group") plus,
+// optionally, one dense group (the shared expert over all tokens):
+//   pass A (kSwiGLU): act = SiLU(x W_gate^T) ⊙ (x W_up^T)     [rows, F]
+//   pass B (kDown):   y   = act W_down^T                       [rows, d]
+// Group sizes live on the device (dispatch offsets); the host never syncs.
+//
+// CTA = 6 warps, one CTA per SM:
+//   warp 0      TMA producer: A tile [128 x 128 B] and B tile [256 x 128 B]
+//               per stage, 128-byte swizzle, 4-stage mbarrier ring
+//   warp 1      tcgen05.mma issuer (one thread), M=128 N=256, fp32 in TMEM;
+//               owns the 512-column TMEM allocation (2 accumulators)
+//   warps 2..5  epilogue: tcgen05.ld from TMEM, SiLU⊙up or plain convert,
+//               16-byte stores; double-buffered accumulators let the epilogue
+//               of one tile overlap the MMAs of the next
+// For pass A the B tile stacks 128 rows of W_gate over the same 128 rows of
+// W_up, so one N=256 MMA produces the gate half (columns 0..127) and the up
+// half (128..255) of a 128-column output tile.
+//
+// Tiles of one group are ordered in bands of at most 16 m-tiles: inside a band
+// the n-tiles advance slowest, so CTAs running side by side share one weight
+// slice (and the band's activations) through L2.
+//
+// Every mbarrier wait is bounded (wall-clock budget). On expiry the kernel
+// records MOE_ERR_TIMEOUT in the status word, lets the other roles stop, waits
+// (bounded) for its own TMA loads and MMAs in flight, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kAccCols = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxGroups = kMaxExperts + 1;
+constexpr int kBandMax = 16;
+constexpr uint32_t kStageA = kBM * 128;   // 128 rows x 128 B
+constexpr uint32_t kStageB = 256 * 128;   // 256 rows x 128 B
+constexpr uint32_t kStageBytes = kStageA + kStageB;
+constexpr size_t kDynSmem = static_cast<size_t>(kStages) * kStageBytes + 1024;
+constexpr uint64_t kWaitBudgetNs = 4000000000ull;   // 4 s per wait
+constexpr uint64_t kDrainBudgetNs = 200000000ull;   // 0.2 s
+
+enum { kSwiGLU = 0, kDown = 1 };
+
+struct GemmParams {
+  const int32_t* offsets;  // [n_routed + 1] row offsets of the routed groups
+  int32_t n_routed;
+  int32_t rows_routed;     // rows of the routed operand (offsets[n_routed] <= this)
+  int32_t rows_shared;     // rows of the dense group (0 = none)
+  int32_t K;               // reduction width of the routed groups
+  int32_t K_shared;        // reduction width of the dense group
+  int32_t n_out;           // output columns of the routed groups
+  int32_t n_out_shared;    // output columns of the dense group
+  void* out;               // [sum rows, n_out]
+  void* out_shared;        // [rows_shared, n_out_shared]
+  int32_t* status;
+  uint64_t budget_ns;
+};
+
+struct TileInfo {
+  int g, m_blk, n_blk, row0, rows, ncols, b_row0, num_kb;
+};
+
+template <int BN, int BK>
+__device__ __forceinline__ TileInfo decode_tile(int tile, const int* tile_start, const int* grp_off,
+                                                int G, const GemmParams& p) {
+  int lo = 0, hi = G;  // tile_start[lo] <= tile < tile_start[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_start[mid] <= tile) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  ti.g = lo;
+  if (lo < p.n_routed) {
+    ti.row0 = grp_off[lo];
+    ti.rows = grp_off[lo + 1] - grp_off[lo];
+    ti.ncols = p.n_out;
+    ti.b_row0 = lo * p.n_out;
+    ti.num_kb = (p.K + BK - 1) / BK;
+  } else {
+    ti.row0 = 0;
+    ti.rows = p.rows_shared;
+    ti.ncols = p.n_out_shared;
+    ti.b_row0 = 0;
+    ti.num_kb = (p.K_shared + BK - 1) / BK;
+  }
+  const int mt = (ti.rows + kBM - 1) / kBM;
+  const int nt = (ti.ncols + BN - 1) / BN;
+  const int nbands0 = (mt + kBandMax - 1) / kBandMax;
+  const int band_sz = (mt + nbands0 - 1) / nbands0;
+  const int l = tile - tile_start[lo];
+  const int band = l / (band_sz * nt);
+  const int r = l - band * band_sz * nt;
+  const int bs = min(band_sz, mt - band * band_sz);
+  ti.n_blk = r / bs;
+  ti.m_blk = band * band_sz + (r - ti.n_blk * bs);
+  return ti;
+}
+
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kDrainBudgetNs) return false;
+  }
+  return true;
+}
+
+// TMEM -> registers, 32 columns of this warp's 32 lanes, waiting in the same
+// asm block so that no use of the results can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Store 32 consecutive values; `valid` = columns left in the output row
+// (a multiple of the 16-byte vector width).
+__device__ __forceinline__ void store32(__nv_bfloat16* dst, const float (&f)[32], int valid) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (q * 8 < valid) {
+      uint4 u;
+      __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) b[i] = __floats2bfloat162_rn(f[q * 8 + 2 * i], f[q * 8 + 2 * i + 1]);
+      *reinterpret_cast<uint4*>(dst + q * 8) = u;
+    }
+  }
+}
+__device__ __forceinline__ void store32(float* dst, const float (&f)[32], int valid) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    if (q * 4 < valid)
+      *reinterpret_cast<float4*>(dst + q * 4) = make_float4(f[q * 4], f[q * 4 + 1], f[q * 4 + 2], f[q * 4 + 3]);
+  }
+}
+
+template <int MODE, typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA0,
+                        const __grid_constant__ CUtensorMap mapB0,
+                        const __grid_constant__ CUtensorMap mapB0u,
+                        const __grid_constant__ CUtensorMap mapA1,
+                        const __grid_constant__ CUtensorMap mapB1,
+                        const __grid_constant__ CUtensorMap mapB1u, const GemmParams p) {
+  constexpr int BK = 128 / static_cast<int>(sizeof(T));   // elements per 128-byte row
+  constexpr int BN = MODE == kSwiGLU ? 128 : 256;         // output columns per tile
+  constexpr uint32_t kIdesc = make_idesc(kBM, 256, sizeof(T) == 2 ? 1u : 2u);
+
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  __shared__ int tile_start[kMaxGroups + 1];
+  __shared__ int grp_off[kMaxGroups + 1];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.n_routed + (p.rows_shared > 0 ? 1 : 0);
+  volatile int* abort_v = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 128);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mapA0);
+      tma_prefetch_desc(&mapB0);
+      if (MODE == kSwiGLU) tma_prefetch_desc(&mapB0u);
+    }
+    for (int g = lane; g <= p.n_routed; g += 32) grp_off[g] = p.offsets[g];
+    __syncwarp();
+    // offsets must start at 0, never decrease and end inside the operand
+    bool bad = lane == 0 && (grp_off[0] != 0 || grp_off[p.n_routed] > p.rows_routed);
+    for (int g = lane; g < p.n_routed; g += 32) bad |= grp_off[g + 1] < grp_off[g];
+    bad = __any_sync(0xffffffffu, bad);
+    if (bad) {
+      if (lane == 0) atomicCAS(p.status, 0, MOE_ERR_DEVICE_CHECK);
+      for (int g = lane; g <= p.n_routed; g += 32) grp_off[g] = 0;
+      __syncwarp();
+    }
+    int carry = 0;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      int tiles = 0;
+      if (g < G) {
+        const int rows = g < p.n_routed ? grp_off[g + 1] - grp_off[g] : p.rows_shared;
+        const int ncols = g < p.n_routed ? p.n_out : p.n_out_shared;
+        tiles = ((rows + kBM - 1) / kBM) * ((ncols + BN - 1) / BN);
+      }
+      int incl = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < G) tile_start[g] = carry + incl - tiles;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[G] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+  const int total = tile_start[G];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued_mask = 0, issued_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+        const bool dense = ti.g >= p.n_routed;
+        const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
+        const void* mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
+        const void* mBu = dense ? static_cast<const void*>(&mapB1u) : static_cast<const void*>(&mapB0u);
+        const int a_row = ti.row0 + ti.m_blk * kBM;
+        const int b_row = ti.b_row0 + ti.n_blk * BN;
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
+          if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_v, p.status, p.budget_ns,
+                                 MOE_ERR_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = smem + stage * kStageBytes;
+          uint8_t* sB = sA + kStageA;
+          mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+          tma_load_2d(sA, mA, &full_bar[stage], kb * BK, a_row);
+          if (MODE == kSwiGLU) {
+            tma_load_2d(sB, mB, &full_bar[stage], kb * BK, b_row);
+            tma_load_2d(sB + kStageB / 2, mBu, &full_bar[stage], kb * BK, b_row);
+          } else {
+            tma_load_2d(sB, mB, &full_bar[stage], kb * BK, b_row);
+          }
+          issued_mask |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kStages; ++s)
+          if ((issued_mask >> s) & 1u) drain_wait(&full_bar[s], (issued_par >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+        if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, abort_v, p.status, p.budget_ns,
+                               MOE_ERR_TIMEOUT)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * kAccCols;
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
+          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_v, p.status, p.budget_ns,
+                                 MOE_ERR_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
+          const uint32_t b_addr = a_addr + kStageA;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sw128_kmajor_desc(a_addr + kk * 32);
+            const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
+            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+            if (sizeof(T) == 2)
+              mma_f16(d_tmem, ad, bd, kIdesc, accum);
+            else
+              mma_tf32(d_tmem, ad, bd, kIdesc, accum);
+          }
+          mma_commit(&empty_bar[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull_bar[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        mma_commit(&drain_bar);
+        drain_wait(&drain_bar, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    const int row_in_tile = quad * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileInfo ti = decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+      if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_v, p.status, p.budget_ns,
+                             MOE_ERR_TIMEOUT))
+        break;
+      tc_fence_after();
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc) * kAccCols;
+      const int row = ti.m_blk * kBM + row_in_tile;
+      const bool row_ok = row < ti.rows;
+      const int col0 = ti.n_blk * BN;
+      const int cols_left = ti.ncols - col0;
+      const bool dense = ti.g >= p.n_routed;
+      T* out = dense ? static_cast<T*>(p.out_shared) + static_cast<size_t>(row) * p.n_out_shared
+                     : static_cast<T*>(p.out) + static_cast<size_t>(ti.row0 + row) * p.n_out;
+      out += col0;
+      if (MODE == kSwiGLU) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t gr[32], ur[32];
+          tmem_ld32_sync(tbase + c, gr);
+          tmem_ld32_sync(tbase + 128 + c, ur);
+          if (row_ok && c < cols_left) {
+            float act[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float gv = __uint_as_float(gr[i]);
+              const float uv = __uint_as_float(ur[i]);
+              act[i] = gv / (1.0f + __expf(-gv)) * uv;
+            }
+            store32(out + c, act, cols_left - c);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t v[32];
+          tmem_ld32_sync(tbase + c, v);
+          if (row_ok && c < cols_left) {
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+            store32(out + c, f, cols_left - c);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// One CTA, one thread: waits on an mbarrier nothing arrives on, bounded.
+__global__ void selftest_wait_kernel(int32_t* status, uint64_t budget_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  volatile int* ab = &abort_flag;
+  (void)mbar_wait_bounded(&bar, 0, ab, status, budget_ns, MOE_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Row-major [rows, inner] tensor, box = [box_rows, 128 bytes], 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* ptr, int dtype, uint64_t inner, uint64_t rows,
+              uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const uint64_t es = static_cast<uint64_t>(elem_size(dtype));
+  cuuint64_t gdim[2] = {inner, rows};
+  cuuint64_t gstride[1] = {inner * es};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      dtype == MOE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUresult r = enc(m, dt, 2, const_cast<void*>(ptr), gdim, gstride, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int MODE, typename T>
+cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid, cudaStream_t stream) {
+  auto kern = grouped_gemm_kernel<MODE, T>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kDynSmem));
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kThreads, kDynSmem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  return cudaGetLastError();
+}
+
+int tiles_bound(int64_t rows_routed, int n_groups, int64_t n_out, int BN, int64_t rows_dense,
+                int64_t n_out_dense) {
+  int64_t b = (rows_routed / kBM + n_groups) * ((n_out + BN - 1) / BN);
+  if (rows_dense > 0) b += ((rows_dense + kBM - 1) / kBM) * ((n_out_dense + BN - 1) / BN);
+  return static_cast<int>(b < 1 ? 1 : (b > (1 << 30) ? (1 << 30) : b));
+}
+
+}  // namespace
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
+  if (a.T == 0) return cudaSuccess;
+  const int64_t R = a.T * a.k;
+  const bool sh = a.F_sh > 0;
+  const int sms = num_sms();
+  CUtensorMap m[6];
+
+  // pass A: act = SiLU(x Wg^T) * (x Wu^T)
+  if (!make_map(&m[0], a.x_disp, a.dtype, a.d, R, kBM)) return cudaErrorInvalidValue;
+  if (!make_map(&m[1], a.W_gate, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&m[2], a.W_up, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, 128)) return cudaErrorInvalidValue;
+  if (sh) {
+    if (!make_map(&m[3], a.h, a.dtype, a.d, a.T, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&m[4], a.Ws_gate, a.dtype, a.d, a.F_sh, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&m[5], a.Ws_up, a.dtype, a.d, a.F_sh, 128)) return cudaErrorInvalidValue;
+  } else {
+    m[3] = m[0]; m[4] = m[1]; m[5] = m[2];
+  }
+  GemmParams pa{};
+  pa.offsets = a.offsets;
+  pa.n_routed = a.N;
+  pa.rows_routed = static_cast<int32_t>(R);
+  pa.rows_shared = sh ? static_cast<int32_t>(a.T) : 0;
+  pa.K = a.d;
+  pa.K_shared = a.d;
+  pa.n_out = a.F;
+  pa.n_out_shared = a.F_sh;
+  pa.out = a.act;
+  pa.out_shared = a.act_sh;
+  pa.status = a.status;
+  pa.budget_ns = kWaitBudgetNs;
+  int grid = tiles_bound(R, a.N, a.F, 128, sh ? a.T : 0, a.F_sh);
+  if (grid > sms) grid = sms;
+  cudaError_t err = a.dtype == MOE_F32 ? launch_gemm<kSwiGLU, float>(m, pa, grid, stream)
+                                       : launch_gemm<kSwiGLU, __nv_bfloat16>(m, pa, grid, stream);
+  if (err != cudaSuccess) return err;
+
+  // pass B: y = act Wd^T
+  if (!make_map(&m[0], a.act, a.dtype, a.F, R, kBM)) return cudaErrorInvalidValue;
+  if (!make_map(&m[1], a.W_down, a.dtype, a.F, static_cast<uint64_t>(a.N) * a.d, 256)) return cudaErrorInvalidValue;
+  m[2] = m[1];
+  if (sh) {
+    if (!make_map(&m[3], a.act_sh, a.dtype, a.F_sh, a.T, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&m[4], a.Ws_down, a.dtype, a.F_sh, a.d, 256)) return cudaErrorInvalidValue;
+    m[5] = m[4];
+  } else {
+    m[3] = m[0]; m[4] = m[1]; m[5] = m[1];
+  }
+  GemmParams pb = pa;
+  pb.K = a.F;
+  pb.K_shared = a.F_sh;
+  pb.n_out = a.d;
+  pb.n_out_shared = a.d;
+  pb.out = a.y_rows;
+  pb.out_shared = a.y_shared;
+  grid = tiles_bound(R, a.N, a.d, 256, sh ? a.T : 0, a.d);
+  if (grid > sms) grid = sms;
+  return a.dtype == MOE_F32 ? launch_gemm<kDown, float>(m, pb, grid, stream)
+                            : launch_gemm<kDown, __nv_bfloat16>(m, pb, grid, stream);
+}
+
+cudaError_t launch_selftest_wait(int32_t* status, uint64_t budget_ns, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 1, 0, stream>>>(status, budget_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

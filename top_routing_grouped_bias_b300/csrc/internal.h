@@ -1,0 +1,124 @@
+// Internal launch interfaces shared by the host API and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 16;
+constexpr int kDispatchTokensPerBlock = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int elem_size(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
+
+// Workspace layout. Every region starts on a 256-byte boundary. The entry
+// points use the prefixes they need: dispatch [status, block_base],
+// expert FFN [status .. act_sh], forward everything.
+struct WsLayout {
+  size_t status, block_base, act, act_sh, offsets, counts, row_token, inv, x_disp, y_rows, y_sh;
+  size_t end_dispatch, end_ffn, total;
+};
+
+inline WsLayout ws_layout(const moe_config& c) {
+  WsLayout L{};
+  const size_t e = static_cast<size_t>(elem_size(c.dtype));
+  const size_t T = static_cast<size_t>(c.T), R = T * static_cast<size_t>(c.k);
+  const size_t nb = (T + kDispatchTokensPerBlock - 1) / kDispatchTokensPerBlock;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  L.status = take(256);
+  L.block_base = take(nb * static_cast<size_t>(c.N) * 4);
+  L.end_dispatch = o;
+  L.act = take(R * static_cast<size_t>(c.ffn) * e);
+  L.act_sh = take(T * static_cast<size_t>(c.ffn_shared) * e);
+  L.end_ffn = o;
+  L.offsets = take(static_cast<size_t>(c.N + 1) * 4);
+  L.counts = take(static_cast<size_t>(c.N) * 4);
+  L.row_token = take(R * 4);
+  L.inv = take(R * 4);
+  L.x_disp = take(R * static_cast<size_t>(c.d) * e);
+  L.y_rows = take(R * static_cast<size_t>(c.d) * e);
+  L.y_sh = take(c.ffn_shared > 0 ? T * static_cast<size_t>(c.d) * e : 0);
+  L.total = o;
+  return L;
+}
+
+// ---- route ----
+struct RouteArgs {
+  const void* h;
+  const void* W_r;
+  const float* b_r;
+  const float* sel_bias;
+  const float* logits_in;
+  float* logits_out;
+  int32_t* idx;
+  float* gate;
+  int64_t T;
+  int32_t d, N, k, score, norm, dtype;
+};
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
+
+// ---- dispatch ----
+struct DispatchArgs {
+  const void* h;
+  const int32_t* idx;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* row_token;
+  int32_t* inv;
+  void* x_disp;
+  int32_t* block_base;  // scratch [nb * N]
+  int32_t* status;      // device status word (index checks)
+  int64_t T;
+  int32_t d, N, k, dtype;
+};
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
+
+// ---- grouped GEMM (gate/up with SwiGLU epilogue, and down) ----
+struct FfnArgs {
+  const void* x_disp;
+  const int32_t* offsets;
+  const void* W_gate;
+  const void* W_up;
+  const void* W_down;
+  void* y_rows;
+  const void* h;
+  const void* Ws_gate;
+  const void* Ws_up;
+  const void* Ws_down;
+  void* y_shared;
+  void* act;     // [T*k, F]
+  void* act_sh;  // [T, F_sh]
+  int32_t* status;
+  int64_t T;
+  int32_t d, N, k, F, F_sh, dtype;
+};
+cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream);
+
+// ---- combine ----
+struct CombineArgs {
+  const void* y_rows;
+  const int32_t* inv;
+  const float* gate;
+  const void* y_shared;
+  void* out;
+  int64_t T;
+  int32_t d, k, dtype;
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+
+cudaError_t launch_selftest_wait(int32_t* status, uint64_t budget_ns, cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace moe
