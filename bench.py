@@ -34,7 +34,7 @@ from top_routing_grouped_bias_b300 import api, synth  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s; grouped-GEMM TFLOP/s & HBM GB/s vs B300 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-KERNELS_PER_FORWARD = 7  # route 1, dispatch 3, grouped GEMM 2, combine 1
+KERNELS_PER_FORWARD = 8  # route 1, dispatch 4, grouped GEMM 2, combine 1
 
 
 # ------------------------------------------------------------ host logic ---
@@ -410,13 +410,14 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mixtral_prefill", choices=list(synth.WORKLOADS))
+    ap.add_argument("--workload", default="mixtral_prefill",
+                    choices=list(synth.WORKLOADS) + list(synth.PROFILE_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    w = synth.WORKLOADS[args.workload]
+    w = {**synth.WORKLOADS, **synth.PROFILE_WORKLOADS}[args.workload]
     if args.impl == "reference":
         line = bench_reference(args, w)
     else:

@@ -125,12 +125,16 @@ def check_selection(idx_gpu, q_ref, k, delta, what=""):
     (k-th vs (k+1)-th) gap is >= delta must match as a set. The rest must be a
     valid choice within delta. Returns the number of ambiguous tokens."""
     T, N = q_ref.shape
+    delta = np.broadcast_to(np.asarray(delta, dtype=np.float64), (T,))
     S_ref = O.select_topk(q_ref, k)
     qs = -np.sort(-q_ref, axis=1)
     top = qs[:, :min(k + 1, N)]
     gaps = top[:, :-1] - top[:, 1:] if top.shape[1] > 1 else np.full((T, 1), np.inf)
     order_amb = (gaps[:, :k].min(axis=1) < delta) if gaps.shape[1] else np.zeros(T, bool)
     set_amb = (gaps[:, k - 1] < delta) if k < N else np.zeros(T, bool)
+    if not delta.any():
+        order_amb[:] = False
+        set_amb[:] = False
     exact = ~order_amb
     bad = np.nonzero((idx_gpu[exact] != S_ref[exact]).any(axis=1))[0]
     assert bad.size == 0, f"{what}: {bad.size} tokens differ, e.g. t={np.nonzero(exact)[0][bad[0]]}"
@@ -140,10 +144,31 @@ def check_selection(idx_gpu, q_ref, k, delta, what=""):
         if not set_amb[t]:
             assert set(sel.tolist()) == set(S_ref[t].tolist()), f"{what}: set differs at t={t}"
         # each chosen expert is at least as good as the k-th best, up to delta
-        assert (q_ref[t, sel] >= qs[t, k - 1] - delta).all(), f"{what}: invalid choice at t={t}"
+        assert (q_ref[t, sel] >= qs[t, k - 1] - delta[t]).all(), f"{what}: invalid choice at t={t}"
         # slots descend up to delta
-        assert (np.diff(q_ref[t, sel]) <= delta).all(), f"{what}: slot order at t={t}"
+        assert (np.diff(q_ref[t, sel]) <= delta[t]).all(), f"{what}: slot order at t={t}"
     return int(order_amb.sum())
+
+
+def e2e_selection_check(idx_gpu, z_ref, z_gpu, w_score, bias, k, what=""):
+    """End-to-end selection: GPU indices against the oracle's selection from
+    exact logits.
+
+    The GPU selects exactly on its own fp32 logits (checked separately), so
+    a decision can differ from the oracle's only where the logit error moves
+    an adjacent gap among the k+1 best scores across zero. The error is known
+    here (z_gpu - z_ref, itself checked against the fp32 summation bound), so
+    a token is ambiguous when a gap is below twice what that error can move:
+    without a bias selection is monotone in z and gaps move by at most
+    2 max_e |dz|; with a bias gaps in q = p + bias move by at most 4 max|dz|
+    (softmax: |dp_i| <= 2 p_i max|dz|) or 0.5 max|dz| (sigmoid: slope <= 1/4),
+    plus the fp32 rounding of q."""
+    dz = np.abs(z_gpu - z_ref).max(axis=1)
+    if bias is None:
+        return check_selection(idx_gpu, z_ref, k, 2 * (2 * dz) + 1e-7, what)
+    c = 4.0 if w_score == O.SOFTMAX else 0.5
+    q = selection_scores(z_ref, w_score, bias)
+    return check_selection(idx_gpu, q, k, 2 * (c * dz) + 4e-6, what)
 
 
 def oracle_gates_from_logits(z_gpu64, idx_gpu, w_score, w_norm):

@@ -9,8 +9,9 @@
 //               base[b][e] = offsets[e] + sum_{b' < b} count[b'][e]
 //   3. permute  per block: per-warp counts, scan over warps, then the rank of
 //               each pair among earlier pairs of the same expert in its warp;
-//               row = base + warp prefix + rank. Writes row_token, inv and
-//               copies h[t] into its k dispatched rows (16-byte vectors).
+//               row = base + warp prefix + rank. Writes row_token and inv.
+//   4. gather   one thread per 16-byte vector of h: reads h[t] once, writes
+//               it to the token's k dispatched rows.
 // The row of (t, e) is offsets[e] + #{t' < t : e in S_t'}, i.e. rows are
 // ordered by (expert, token).
 #include <cuda_bf16.h>
@@ -100,13 +101,11 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(DispatchArgs a, int
   }
 }
 
-template <typename T>
 __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
   extern __shared__ int sm[];
   const int N = a.N, k = a.k;
   int* whist = sm;                                   // [kWarps][N]
   int* sidx = sm + kWarps * N;                       // [kWarps][32][k]
-  int* srow = sidx + kWarps * 32 * k;                // [kWarps][32][k]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kWarps * N; i += blockDim.x) whist[i] = 0;
   __syncthreads();
@@ -137,7 +136,6 @@ __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
       const int e = my_idx[j];
       if (e < 0) {
         a.inv[t * k + j] = -1;
-        srow[(warp * 32 + lane) * k + j] = -1;
         continue;
       }
       int rank = 0;
@@ -146,26 +144,25 @@ __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
       const int row = whist[warp * N + e] + rank;
       a.row_token[row] = static_cast<int32_t>(t);
       a.inv[t * k + j] = row;
-      srow[(warp * 32 + lane) * k + j] = row;
     }
   }
-  __syncwarp();
-  if (a.x_disp == nullptr) return;
-  // gather: each warp copies its 32 tokens' rows into their k dispatched rows
+}
+
+// Gather: one thread per 16-byte vector of h; it reads h[t] once and writes
+// the vector into each of the token's k dispatched rows (coalesced along d).
+template <typename T>
+__global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a) {
   const int nvec = a.d * static_cast<int>(sizeof(T)) / 16;
-  const uint4* H = static_cast<const uint4*>(a.h);
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= a.T * nvec) return;
+  const int64_t t = i / nvec;
+  const int v = static_cast<int>(i - t * nvec);
+  const uint4 val = static_cast<const uint4*>(a.h)[i];
   uint4* X = static_cast<uint4*>(a.x_disp);
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTB + warp * 32;
-  for (int l = 0; l < 32; ++l) {
-    const int64_t tt = t0 + l;
-    if (tt >= a.T) break;
-    const int* rows = srow + (warp * 32 + l) * k;
-    const uint4* src = H + tt * nvec;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 val = src[v];
-      for (int j = 0; j < k; ++j)
-        if (rows[j] >= 0) X[static_cast<int64_t>(rows[j]) * nvec + v] = val;
-    }
+  const int64_t R = a.T * a.k;
+  for (int j = 0; j < a.k; ++j) {
+    const int64_t row = a.inv[t * a.k + j];
+    if (row >= 0 && row < R) X[row * nvec + v] = val;
   }
 }
 
@@ -180,18 +177,20 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
   const int nb = static_cast<int>((a.T + kTB - 1) / kTB);
   dispatch_count_kernel<<<nb, kTB, a.N * sizeof(int), stream>>>(a);
   dispatch_scan_kernel<<<1, 1024, 0, stream>>>(a, nb);
-  const size_t smem = sizeof(int) * (static_cast<size_t>(kWarps) * a.N + 2u * kWarps * 32 * a.k);
-  cudaError_t err;
-  if (a.dtype == MOE_F32) {
-    err = cudaFuncSetAttribute(dispatch_permute_kernel<float>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    dispatch_permute_kernel<float><<<nb, kTB, smem, stream>>>(a);
-  } else {
-    err = cudaFuncSetAttribute(dispatch_permute_kernel<__nv_bfloat16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    dispatch_permute_kernel<__nv_bfloat16><<<nb, kTB, smem, stream>>>(a);
+  const size_t smem = sizeof(int) * (static_cast<size_t>(kWarps) * a.N + kWarps * 32 * a.k);
+  cudaError_t err = cudaFuncSetAttribute(dispatch_permute_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  dispatch_permute_kernel<<<nb, kTB, smem, stream>>>(a);
+  if (a.x_disp != nullptr) {
+    const int vec = a.dtype == MOE_F32 ? 4 : 8;
+    const int64_t total = a.T * (a.d / vec);
+    const unsigned grid = static_cast<unsigned>((total + 255) / 256);
+    if (a.dtype == MOE_F32)
+      dispatch_gather_kernel<float><<<grid, 256, 0, stream>>>(a);
+    else
+      dispatch_gather_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a);
   }
   return cudaGetLastError();
 }

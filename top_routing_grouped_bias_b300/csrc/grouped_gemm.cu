@@ -446,8 +446,9 @@ bool make_map(CUtensorMap* m, const void* ptr, int dtype, uint64_t inner, uint64
   cuuint64_t gstride[1] = {inner * es};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), box_rows};
   cuuint32_t estr[2] = {1, 1};
+  // fp32 operands are rounded to tf32 by the TMA unit on the way to shared memory
   const CUtensorMapDataType dt =
-      dtype == MOE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      dtype == MOE_F32 ? CU_TENSOR_MAP_DATA_TYPE_TFLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUresult r = enc(m, dt, 2, const_cast<void*>(ptr), gdim, gstride, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -81,6 +81,15 @@ WORKLOADS = {
 }
 
 
+# Reduced cases of the same kernels for profiler captures: weights still
+# larger than L2, a few hundred MB of activations.
+PROFILE_WORKLOADS = {
+    "prof_prefill": Workload("prof_prefill", T=2048, d=4096, N=2, F=14336, k=2),
+    "prof_fine_grained": Workload("prof_fine_grained", T=2048, d=7168, N=64, F=2048, k=8,
+                                  F_sh=2048, score="sigmoid", bias_zipf_s=1.1),
+}
+
+
 def _randn(gen: torch.Generator, shape, std: float, dtype: torch.dtype,
            device) -> torch.Tensor:
     """N(0, std) drawn in fp32 on ``device`` then rounded to ``dtype``.
