@@ -121,6 +121,31 @@ moe_status moe_dispatch(const moe_config* cfg, const void* h, const int32_t* idx
                         int32_t* inv, void* x_disp,
                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Dispatch for callers that cannot allocate device memory. The pages have no
+ * counterpart to this entry point; it exists for callers that have no device
+ * allocator to provide moe_dispatch's workspace (a plain C/C++ host program
+ * embedding the library without a framework, or a runtime that forbids device
+ * allocation after start-up because it can synchronise the device or exceed a
+ * fixed memory budget).
+ *   Same arguments, layouts and results as moe_dispatch, without the
+ *   workspace. The per-block histograms live in a fixed array inside the
+ *   library's device image (1 MiB + 256 B, reserved on every GPU that loads
+ *   the library until the process exits). Nothing is allocated: no cudaMalloc,
+ *   no cudaFree, no allocating library routine.
+ *   Limit: ceil(T / 256) * N <= 262144 (e.g. T <= 65536 with N <= 1024);
+ *   larger requests return MOE_ERR_WORKSPACE before anything is launched.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   All calls share the one array: calls whose work overlaps on the GPU (on
+ *   different streams, or from several host threads) race and corrupt each
+ *   other's results. Serialise them. Out-of-range expert indices are skipped
+ *   as in moe_dispatch; this variant has no device status read-out.
+ */
+moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* h, const int32_t* idx,
+                                int32_t* counts, int32_t* offsets, int32_t* row_token,
+                                int32_t* inv, void* x_disp, cudaStream_t stream);
+
 /* Stage 5+6: every expert's SwiGLU FFN over its dispatched rows, as one
  * grouped GEMM pair on the tensor cores (tcgen05, TMA-fed).
  * [P1] §一 E_i(h) = W_down (SiLU(W_gate h) * W_up h); [P1] §十二 Grouped GEMM;

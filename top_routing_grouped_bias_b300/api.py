@@ -32,6 +32,7 @@ NORMS = {"selected": 0, "none": 1}
 ENTRY_POINTS = (
     "moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
     "moe_forward", "moe_read_status", "moe_selftest_wait_timeout", "moe_status_string",
+    "moe_dispatch_noalloc",
 )
 
 
@@ -65,6 +66,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_workspace_size.restype = _sz
     lib.moe_route.argtypes = [cfgp] + [_vp] * 8 + [_vp, _sz, _vp]
     lib.moe_dispatch.argtypes = [cfgp] + [_vp] * 7 + [_vp, _sz, _vp]
+    lib.moe_dispatch_noalloc.argtypes = [cfgp] + [_vp] * 7 + [_vp]
     lib.moe_expert_ffn.argtypes = [cfgp] + [_vp] * 11 + [_vp, _sz, _vp]
     lib.moe_combine.argtypes = [cfgp] + [_vp] * 5 + [_vp]
     lib.moe_forward.argtypes = [cfgp] + [_vp] * 15 + [_vp, _sz, _vp]
@@ -137,6 +139,16 @@ def moe_dispatch(cfg, h, idx, counts, offsets, row_token, inv, x_disp, ws, strea
     s = load().moe_dispatch(ctypes.byref(cfg), _p(h), _p(idx), _p(counts), _p(offsets),
                             _p(row_token), _p(inv), _p(x_disp), _p(ws), ws.numel(), _stream(stream))
     _check(s, "moe_dispatch")
+
+
+def moe_dispatch_noalloc(cfg, h, idx, counts, offsets, row_token, inv, x_disp, stream=None):
+    """moe_dispatch without a workspace, for callers that cannot allocate
+    device memory: the library keeps the scratch in a fixed array of its own
+    (at most ceil(T/256) * N = 262144 histogram entries). Calls that overlap
+    on the GPU share that array and race."""
+    s = load().moe_dispatch_noalloc(ctypes.byref(cfg), _p(h), _p(idx), _p(counts), _p(offsets),
+                                    _p(row_token), _p(inv), _p(x_disp), _stream(stream))
+    _check(s, "moe_dispatch_noalloc")
 
 
 def moe_expert_ffn(cfg, x_disp, offsets, W_gate, W_up, W_down, y_rows, h=None, Ws_gate=None,

@@ -17,7 +17,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libmoe_b300.so")
-SOURCES = ["api.cu", "route.cu", "dispatch.cu", "combine.cu", "grouped_gemm.cu"]
+SOURCES = ["api.cu", "route.cu", "dispatch.cu", "combine.cu", "grouped_gemm.cu",
+           "dispatch_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
