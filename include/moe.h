@@ -96,6 +96,10 @@ size_t moe_workspace_size(const moe_config* cfg);
  *   idx        [T, k] int32 out: selected experts, by descending selection
  *              score; equal scores go to the lower expert index first
  *   gate       [T, k] fp32 out: gate weight of each selected expert
+ *   ws         optional (may be NULL): when given, device-side failures are
+ *              recorded in its status word
+ * bf16 routing from h with N <= 256 runs on the tensor cores (fp32
+ * accumulation); fp32 inputs, N > 256 and routing from logits run on CUDA cores.
  */
 moe_status moe_route(const moe_config* cfg, const void* h, const void* W_r,
                      const float* b_r, const float* sel_bias,

@@ -291,3 +291,34 @@ def test_zero_weight_routed_experts_leave_shared_only(cuda_lib):
     r = run_forward(cfg, gpu_inputs(inp))
     ref = O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"])
     assert_close_tol(np_f(r["out"]), ref, BF16_TOL, "shared only")
+
+
+@pytest.mark.parametrize("score", ["softmax", "sigmoid"])
+@pytest.mark.parametrize("N,k", [(16, 4), (128, 1), (256, 8), (40, 16)])
+def test_route_tensor_core_exact_ties(cuda_lib, score, N, k):
+    """bf16 routing from h runs as a tcgen05 GEMM with a top-k epilogue.
+    Duplicated router rows give bitwise-equal logits; the lower expert index
+    must come first, exactly as the oracle orders equal scores."""
+    T, d = 300, 256
+    gen = torch.Generator().manual_seed(N + k)
+    h = torch.randn((T, d), generator=gen).to(torch.bfloat16)
+    W = (torch.randn((N, d), generator=gen) * 0.05).to(torch.bfloat16)
+    for a, b in ((0, 1), (2, 5), (N - 1, 3), (N // 2, N // 2 + 1)):
+        W[b] = W[a]
+    cfg = api.make_config(T, d, N, k, 64, score=score)
+    dev = "cuda"
+    ws = api.alloc_workspace(cfg, dev)
+    logits = torch.empty((T, N), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, k), dtype=torch.float32, device=dev)
+    api.moe_route(cfg, h.to(dev), W.to(dev), None, None, None, logits, idx, gate, ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    z = np_f(logits)
+    for a, b in ((0, 1), (2, 5), (N - 1, 3), (N // 2, N // 2 + 1)):
+        assert (z[:, a] == z[:, b]).all()
+    S, g, _, _ = O.route(z, k, score, "selected")
+    assert (np_i(idx) == S).all()
+    np.testing.assert_allclose(np_f(gate), g, atol=1e-6, rtol=0)
+    bound = logit_bound(to_f64(h), to_f64(W))
+    assert (np.abs(z - O.router_logits(to_f64(h), to_f64(W))) <= bound).all()

@@ -45,7 +45,7 @@ P* at(void* ws, size_t off) {
 
 moe_status route_impl(const moe_config* cfg, const void* h, const void* W_r, const float* b_r,
                       const float* sel_bias, const float* logits_in, float* logits_out,
-                      int32_t* idx, float* gate, cudaStream_t stream) {
+                      int32_t* idx, float* gate, int32_t* status, cudaStream_t stream) {
   if (h != nullptr) {
     if (!ok_tensor(h) || !ok_tensor(W_r)) return MOE_ERR_INVALID_ARG;
   } else if (!ok_f32(logits_in)) {
@@ -59,6 +59,7 @@ moe_status route_impl(const moe_config* cfg, const void* h, const void* W_r, con
   a.h = h; a.W_r = W_r; a.b_r = b_r; a.sel_bias = sel_bias; a.logits_in = logits_in;
   a.logits_out = logits_out; a.idx = idx; a.gate = gate; a.T = cfg->T; a.d = cfg->d;
   a.N = cfg->N; a.k = cfg->k; a.score = cfg->score; a.norm = cfg->norm; a.dtype = cfg->dtype;
+  a.status = status;
   return from_cuda(launch_route(a, stream));
 }
 
@@ -124,11 +125,13 @@ size_t moe_workspace_size(const moe_config* cfg) {
 moe_status moe_route(const moe_config* cfg, const void* h, const void* W_r, const float* b_r,
                      const float* sel_bias, const float* logits_in, float* logits_out,
                      int32_t* idx, float* gate, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   moe_status s = check_config(cfg);
   if (s != MOE_OK) return s;
-  return route_impl(cfg, h, W_r, b_r, sel_bias, logits_in, logits_out, idx, gate, stream);
+  // the workspace is optional here; when given, its status word records
+  // device-side failures of the router's bounded waits
+  int32_t* status = (ws != nullptr && ws_bytes >= 256 && aligned(ws, 256))
+                        ? static_cast<int32_t*>(ws) : nullptr;
+  return route_impl(cfg, h, W_r, b_r, sel_bias, logits_in, logits_out, idx, gate, status, stream);
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const void* h, const int32_t* idx, int32_t* counts,
@@ -187,7 +190,8 @@ moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r, co
   void* y_rows = at<void>(ws, L.y_rows);
   void* y_sh = cfg->ffn_shared > 0 ? at<void>(ws, L.y_sh) : nullptr;
 
-  s = route_impl(cfg, h, W_r, b_r, sel_bias, nullptr, logits_out, idx, gate, stream);
+  s = route_impl(cfg, h, W_r, b_r, sel_bias, nullptr, logits_out, idx, gate,
+                 at<int32_t>(ws, L.status), stream);
   if (s != MOE_OK) return s;
   s = dispatch_impl(cfg, h, idx, cnt, offsets, row_token, inv, x_disp, ws, L, stream);
   if (s != MOE_OK) return s;

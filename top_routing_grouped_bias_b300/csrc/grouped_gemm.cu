@@ -22,6 +22,11 @@
 // W_up, so one N=256 MMA produces the gate half (columns 0..127) and the up
 // half (128..255) of a 128-column output tile.
 //
+// A third instance (kRoute) is the router: logits = h W_r^T for 128 tokens per
+// tile with all N <= 256 experts in one accumulator; its epilogue gives each
+// thread one token's logit row straight from TMEM and does softmax / sigmoid,
+// the selection bias, the top-k with the lowest-index tie-break and the gates.
+//
 // Tiles of one group are ordered in bands of at most 16 m-tiles: inside a band
 // the n-tiles advance slowest, so CTAs running side by side share one weight
 // slice (and the band's activations) through L2.
@@ -53,7 +58,17 @@ constexpr size_t kDynSmem = static_cast<size_t>(kStages) * kStageBytes + 1024;
 constexpr uint64_t kWaitBudgetNs = 4000000000ull;   // 4 s per wait
 constexpr uint64_t kDrainBudgetNs = 200000000ull;   // 0.2 s
 
-enum { kSwiGLU = 0, kDown = 1 };
+enum { kSwiGLU = 0, kDown = 1, kRoute = 2 };
+
+// Router epilogue arguments (kRoute only).
+struct RouteEpi {
+  const float* b_r;       // [N] or null
+  const float* sel_bias;  // [N] or null
+  float* logits_out;      // [T, N] or null
+  int32_t* idx;           // [T, k]
+  float* gate;            // [T, k]
+  int32_t N, k, score, norm;
+};
 
 struct GemmParams {
   const int32_t* offsets;  // [n_routed + 1] row offsets of the routed groups
@@ -68,6 +83,7 @@ struct GemmParams {
   void* out_shared;        // [rows_shared, n_out_shared]
   int32_t* status;
   uint64_t budget_ns;
+  RouteEpi re;
 };
 
 struct TileInfo {
@@ -157,7 +173,140 @@ __device__ __forceinline__ void store32(float* dst, const float (&f)[32], int va
   }
 }
 
-template <int MODE, typename T>
+// Keeps the KT best (score, index) pairs in descending order. Candidates
+// arrive in ascending expert order and displace only on a strictly larger
+// score, so equal scores keep the lower index first.
+template <int KT>
+struct TopK {
+  float v[KT];
+  float z[KT];
+  int i[KT];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int j = 0; j < KT; ++j) {
+      v[j] = -INFINITY;
+      z[j] = 0.f;
+      i[j] = 0x7fffffff;
+    }
+  }
+  __device__ __forceinline__ void push(float q, int e, float ze) {
+    if (!(q > v[KT - 1])) return;
+    v[KT - 1] = q;
+    i[KT - 1] = e;
+    z[KT - 1] = ze;
+#pragma unroll
+    for (int j = KT - 1; j > 0; --j) {
+      if (v[j] > v[j - 1]) {
+        const float tv = v[j]; v[j] = v[j - 1]; v[j - 1] = tv;
+        const float tz = z[j]; z[j] = z[j - 1]; z[j - 1] = tz;
+        const int ti = i[j]; i[j] = i[j - 1]; i[j - 1] = ti;
+      }
+    }
+  }
+};
+
+// One thread = one token: its logits are TMEM lane `row_in_tile`, columns
+// [0, N). Passes over TMEM: (A) logits, their max, and without a bias the
+// top-k on the logits (softmax and sigmoid are monotone); (B) softmax
+// denominator when needed; (C) with a bias, the top-k on p + bias.
+template <int KT>
+__device__ __forceinline__ void route_epilogue(uint32_t tbase, int64_t row, bool valid, int n_pad,
+                                               const RouteEpi& r) {
+  const int N = r.N;
+  const bool bias = r.sel_bias != nullptr;
+  const bool softmax = r.score == MOE_SCORE_SOFTMAX;
+  TopK<KT> top;
+  top.init();
+  float m = -INFINITY;
+  float* zrow = r.logits_out != nullptr ? r.logits_out + row * N : nullptr;
+#pragma unroll 1
+  for (int c = 0; c < n_pad; c += 32) {
+    uint32_t v[32];
+    tmem_ld32_sync(tbase + c, v);
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int e = c + i;
+        if (e < N) {
+          const float z = __uint_as_float(v[i]) + (r.b_r != nullptr ? r.b_r[e] : 0.f);
+          if (zrow != nullptr) zrow[e] = z;
+          m = fmaxf(m, z);
+          if (!bias) top.push(z, e, z);
+        }
+      }
+    }
+  }
+  float s = 0.f;
+  if (softmax && (bias || r.norm == MOE_NORM_NONE)) {
+#pragma unroll 1
+    for (int c = 0; c < n_pad; c += 32) {
+      uint32_t v[32];
+      tmem_ld32_sync(tbase + c, v);
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = c + i;
+          if (e < N) {
+            const float z = __uint_as_float(v[i]) + (r.b_r != nullptr ? r.b_r[e] : 0.f);
+            s += expf(z - m);
+          }
+        }
+      }
+    }
+  }
+  if (bias) {
+#pragma unroll 1
+    for (int c = 0; c < n_pad; c += 32) {
+      uint32_t v[32];
+      tmem_ld32_sync(tbase + c, v);
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = c + i;
+          if (e < N) {
+            const float z = __uint_as_float(v[i]) + (r.b_r != nullptr ? r.b_r[e] : 0.f);
+            const float pe = softmax ? expf(z - m) / s : 1.f / (1.f + expf(-z));
+            top.push(pe + r.sel_bias[e], e, z);
+          }
+        }
+      }
+    }
+  }
+  if (!valid) return;
+  const int k = r.k;
+  float g[KT];
+  float den = 0.f;
+  if (softmax && r.norm == MOE_NORM_SELECTED) {
+    float ms = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < KT; ++j)
+      if (j < k) ms = fmaxf(ms, top.z[j]);
+#pragma unroll
+    for (int j = 0; j < KT; ++j) {
+      g[j] = j < k ? expf(top.z[j] - ms) : 0.f;
+      den += g[j];
+    }
+  } else if (softmax) {
+#pragma unroll
+    for (int j = 0; j < KT; ++j) g[j] = j < k ? expf(top.z[j] - m) / s : 0.f;
+  } else {
+#pragma unroll
+    for (int j = 0; j < KT; ++j) {
+      g[j] = j < k ? 1.f / (1.f + expf(-top.z[j])) : 0.f;
+      den += g[j];
+    }
+  }
+  const bool renorm = r.norm == MOE_NORM_SELECTED;
+#pragma unroll
+  for (int j = 0; j < KT; ++j) {
+    if (j < k) {
+      r.idx[row * k + j] = top.i[j] == 0x7fffffff ? 0 : top.i[j];
+      r.gate[row * k + j] = renorm ? g[j] / den : g[j];
+    }
+  }
+}
+
+template <int MODE, typename T, int KT = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA0,
                         const __grid_constant__ CUtensorMap mapB0,
@@ -167,7 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mapB1u, const GemmParams p) {
   constexpr int BK = 128 / static_cast<int>(sizeof(T));   // elements per 128-byte row
   constexpr int BN = MODE == kSwiGLU ? 128 : 256;         // output columns per tile
-  constexpr uint32_t kIdesc = make_idesc(kBM, 256, sizeof(T) == 2 ? 1u : 2u);
+  // kRoute: one accumulator of n_out = N rounded up to 16 columns
+  const int mma_n = MODE == kRoute ? p.n_out : 256;
+  const uint32_t idesc = make_idesc(kBM, mma_n, sizeof(T) == 2 ? 1u : 2u);
+  const uint32_t stage_tx = MODE == kRoute ? kStageA + static_cast<uint32_t>(mma_n) * 128u : kStageBytes;
 
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -209,14 +361,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&mapB0);
       if (MODE == kSwiGLU) tma_prefetch_desc(&mapB0u);
     }
-    for (int g = lane; g <= p.n_routed; g += 32) grp_off[g] = p.offsets[g];
+    if (MODE == kRoute) {
+      if (lane == 0) { grp_off[0] = 0; grp_off[1] = p.rows_routed; }
+    } else {
+      for (int g = lane; g <= p.n_routed; g += 32) grp_off[g] = p.offsets[g];
+    }
     __syncwarp();
     // offsets must start at 0, never decrease and end inside the operand
     bool bad = lane == 0 && (grp_off[0] != 0 || grp_off[p.n_routed] > p.rows_routed);
     for (int g = lane; g < p.n_routed; g += 32) bad |= grp_off[g + 1] < grp_off[g];
     bad = __any_sync(0xffffffffu, bad);
     if (bad) {
-      if (lane == 0) atomicCAS(p.status, 0, MOE_ERR_DEVICE_CHECK);
+      if (lane == 0 && p.status != nullptr) atomicCAS(p.status, 0, MOE_ERR_DEVICE_CHECK);
       for (int g = lane; g <= p.n_routed; g += 32) grp_off[g] = 0;
       __syncwarp();
     }
@@ -268,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sA = smem + stage * kStageBytes;
           uint8_t* sB = sA + kStageA;
-          mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+          mbar_arrive_expect_tx(&full_bar[stage], stage_tx);
           tma_load_2d(sA, mA, &full_bar[stage], kb * BK, a_row);
           if (MODE == kSwiGLU) {
             tma_load_2d(sB, mB, &full_bar[stage], kb * BK, b_row);
@@ -319,9 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
             const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
             if (sizeof(T) == 2)
-              mma_f16(d_tmem, ad, bd, kIdesc, accum);
+              mma_f16(d_tmem, ad, bd, idesc, accum);
             else
-              mma_tf32(d_tmem, ad, bd, kIdesc, accum);
+              mma_tf32(d_tmem, ad, bd, idesc, accum);
           }
           mma_commit(&empty_bar[stage]);
           if (++stage == kStages) {
@@ -363,7 +519,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       T* out = dense ? static_cast<T*>(p.out_shared) + static_cast<size_t>(row) * p.n_out_shared
                      : static_cast<T*>(p.out) + static_cast<size_t>(ti.row0 + row) * p.n_out;
       out += col0;
-      if (MODE == kSwiGLU) {
+      if (MODE == kRoute) {
+        route_epilogue<KT>(tbase, row, row_ok, p.n_out, p.re);
+      } else if (MODE == kSwiGLU) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           uint32_t gr[32], ur[32];
@@ -455,9 +613,9 @@ bool make_map(CUtensorMap* m, const void* ptr, int dtype, uint64_t inner, uint64
   return r == CUDA_SUCCESS;
 }
 
-template <int MODE, typename T>
+template <int MODE, typename T, int KT = 1>
 cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid, cudaStream_t stream) {
-  auto kern = grouped_gemm_kernel<MODE, T>;
+  auto kern = grouped_gemm_kernel<MODE, T, KT>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kDynSmem));
   if (err != cudaSuccess) return err;
@@ -547,6 +705,47 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   if (grid > sms) grid = sms;
   return a.dtype == MOE_F32 ? launch_gemm<kDown, float>(m, pb, grid, stream)
                             : launch_gemm<kDown, __nv_bfloat16>(m, pb, grid, stream);
+}
+
+bool route_on_tensor_cores(const RouteArgs& a) {
+  return a.h != nullptr && a.dtype == MOE_BF16 && a.N <= 256;
+}
+
+cudaError_t launch_route_mma(const RouteArgs& a, cudaStream_t stream) {
+  const int n_pad = (a.N + 15) / 16 * 16;
+  CUtensorMap m[6];
+  if (!make_map(&m[0], a.h, a.dtype, a.d, a.T, kBM)) return cudaErrorInvalidValue;
+  if (!make_map(&m[1], a.W_r, a.dtype, a.d, a.N, static_cast<uint32_t>(n_pad)))
+    return cudaErrorInvalidValue;
+  m[2] = m[1]; m[3] = m[0]; m[4] = m[1]; m[5] = m[1];
+  GemmParams p{};
+  p.offsets = nullptr;
+  p.n_routed = 1;
+  p.rows_routed = static_cast<int32_t>(a.T);
+  p.rows_shared = 0;
+  p.K = a.d;
+  p.K_shared = a.d;
+  p.n_out = n_pad;
+  p.n_out_shared = 0;
+  p.status = a.status;
+  p.budget_ns = kWaitBudgetNs;
+  p.re.b_r = a.b_r;
+  p.re.sel_bias = a.sel_bias;
+  p.re.logits_out = a.logits_out;
+  p.re.idx = a.idx;
+  p.re.gate = a.gate;
+  p.re.N = a.N;
+  p.re.k = a.k;
+  p.re.score = a.score;
+  p.re.norm = a.norm;
+  int grid = static_cast<int>((a.T + kBM - 1) / kBM);
+  if (grid > num_sms()) grid = num_sms();
+  using bf = __nv_bfloat16;
+  if (a.k <= 1) return launch_gemm<kRoute, bf, 1>(m, p, grid, stream);
+  if (a.k <= 2) return launch_gemm<kRoute, bf, 2>(m, p, grid, stream);
+  if (a.k <= 4) return launch_gemm<kRoute, bf, 4>(m, p, grid, stream);
+  if (a.k <= 8) return launch_gemm<kRoute, bf, 8>(m, p, grid, stream);
+  return launch_gemm<kRoute, bf, 16>(m, p, grid, stream);
 }
 
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t budget_ns, cudaStream_t stream) {

@@ -63,10 +63,14 @@ struct RouteArgs {
   float* logits_out;
   int32_t* idx;
   float* gate;
+  int32_t* status;  // device status word or null
   int64_t T;
   int32_t d, N, k, score, norm, dtype;
 };
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
+// Router as a tcgen05 GEMM with a top-k epilogue (bf16, N <= 256, from h).
+bool route_on_tensor_cores(const RouteArgs& a);
+cudaError_t launch_route_mma(const RouteArgs& a, cudaStream_t stream);
 
 // ---- dispatch ----
 struct DispatchArgs {

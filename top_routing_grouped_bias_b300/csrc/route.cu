@@ -1,4 +1,7 @@
 // Router: logits, scores, top-k selection and gates, one warp per token.
+// This SIMT kernel serves fp32 inputs, N > 256 experts and routing from given
+// logits; bf16 routing from h with N <= 256 runs as a tcgen05 GEMM with the
+// same selection rules in its epilogue (grouped_gemm.cu, kRoute).
 //
 // Pages: "MOE 专家选择与路由机制" §二 (z = W_r h + b_r; softmax; TopK; renormalise
 // over the selected experts); "MoE：router 怎样选 expert" (softmax over the
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
+  if (route_on_tensor_cores(a)) return launch_route_mma(a, stream);
   const size_t smem = static_cast<size_t>(kRouteWarps) * a.N * (a.sel_bias ? 2 : 1) * sizeof(float);
   const unsigned grid = static_cast<unsigned>((a.T + kRouteWarps - 1) / kRouteWarps);
   cudaError_t err;
