@@ -333,3 +333,47 @@ def topk_by_subsets(q_row, k):
         if best is None or key < best:
             best = key
     return set(best[1])
+
+
+# --------------------------------------------------------------------------
+# Routing side statistics
+# --------------------------------------------------------------------------
+def router_probabilities(z, score_kind):
+    """Per-token distribution over experts used by the balance statistics.
+
+    Softmax router: p = softmax(z). Sigmoid router: the scores divided by
+    their sum over all experts, so that each row sums to 1 (reading taken:
+    the pages define the statistics with router probabilities, and a sigmoid
+    router's scores are not a distribution until normalised)."""
+    if score_kind == SOFTMAX:
+        return softmax(z)
+    s = sigmoid(z)
+    return s / s.sum(axis=-1, keepdims=True)
+
+
+def logsumexp(z):
+    z = np.asarray(z, dtype=np.float64)
+    m = z.max(axis=-1, keepdims=True)
+    return (m + np.log(np.exp(z - m).sum(axis=-1, keepdims=True)))[..., 0]
+
+
+def routing_stats(z, S, score_kind, N):
+    """Balance and stability statistics of one routing decision.
+
+    [P1] §五: f_i = share of routed (token, slot) pairs sent to expert i,
+    P_i = mean router probability of expert i, L_balance = N * sum_i f_i P_i
+    (equal to 1 when both are uniform); router z-loss
+    L_z = (1/T) sum_t (log sum_i exp z_{t,i})^2. [P1] §十三 lists the per-expert
+    load and the routing entropy among the quantities to monitor:
+    H = (1/T) sum_t -sum_i p_{t,i} log p_{t,i}.
+    Returns a dict with L_bal, L_z, entropy, P [N], f [N]."""
+    z = np.asarray(z, dtype=np.float64)
+    S = np.asarray(S)
+    T, k = S.shape
+    p = router_probabilities(z, score_kind)
+    P = p.mean(axis=0)
+    f = np.bincount(S.reshape(-1), minlength=N).astype(np.float64) / (T * k)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        plogp = np.where(p > 0, p * np.log(p), 0.0)
+    return dict(L_bal=float(N * np.sum(f * P)), L_z=float(np.mean(logsumexp(z) ** 2)),
+                entropy=float(np.mean(-plogp.sum(axis=-1))), P=P, f=f)

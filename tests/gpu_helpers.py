@@ -7,11 +7,14 @@ Tolerances (derived in the design notes):
 * gates: 1e-6 absolute against the oracle fed the GPU's own logits;
 * logits: |z_gpu - z| <= d * 2^-24 * sum_i |h_i W_i| + 1e-6 (fp32 summation of
   exact bf16 products, any order);
-* combine: one rounding to the output dtype: |out - ref| <= 2^-8 |ref| + 1e-6
-  (bf16) or 1e-6 (|ref| + 1) (fp32), ref = the oracle's combine of the GPU's
-  own y_rows and gates;
+* combine: one rounding to the output dtype of an fp32 sum with error E:
+  |out - ref| <= 2^-8 (|ref| + E) + E (bf16), ref = the oracle's combine of
+  the GPU's own y_rows and gates;
 * layer output and expert rows: bf16 max-abs <= 2e-2 and rel-L2 <= 5e-3;
-  fp32 (tf32 tensor cores) max-abs <= 1e-2 and rel-L2 <= 2e-3.
+  fp32 (tf32 tensor cores) max-abs <= 1e-2 and rel-L2 <= 2e-3. On the small
+  synthetic cases an output element may instead meet the bf16 bound derived
+  in assert_layer_close (outputs of magnitude >= ~2.5 cannot meet 2e-2 after
+  three bf16 roundings); the named workloads use the stated bound alone.
 """
 from __future__ import annotations
 
@@ -43,6 +46,25 @@ def assert_close_tol(got, ref, tol, what=""):
     assert max_abs <= tol["max_abs"], f"{what}: max-abs {max_abs:.3e} > {tol['max_abs']}"
     assert rel_l2 <= tol["rel_l2"], f"{what}: rel-L2 {rel_l2:.3e} > {tol['rel_l2']}"
     return max_abs, rel_l2
+
+
+def assert_layer_close(got, ref, mag, tol, what=""):
+    """Layer output check for synthetic cases whose outputs can exceed the
+    range where the stated absolute bound is reachable in bf16. An element
+    passes when it meets the stated max-abs bound OR the bf16 bound derived
+    from the arithmetic: one rounding of the output (2^-8 |ref|) plus one of
+    each bf16 intermediate that enters it (2^-8 of mag = |y_shared| +
+    sum_j g_j |y_j|) plus the bf16 activation (2^-9 mag). rel-L2 must meet
+    the stated bound over the whole tensor."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(got - ref)
+    derived = 2.0 ** -8 * (np.abs(ref) + mag) + 2.0 ** -9 * mag + 1e-3
+    bad = err > np.maximum(tol["max_abs"], derived)
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond both bounds, max err {err.max():.3e}"
+    rel_l2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+    assert rel_l2 <= tol["rel_l2"], f"{what}: rel-L2 {rel_l2:.3e} > {tol['rel_l2']}"
+    return float(err.max()), rel_l2
 
 
 def np_i(t):

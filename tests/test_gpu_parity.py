@@ -6,7 +6,8 @@ import pytest
 import torch
 
 from conftest import load_golden
-from gpu_helpers import (BF16_TOL, F32_TOL, assert_close_tol, check_combine, check_selection,
+from gpu_helpers import (BF16_TOL, F32_TOL, assert_close_tol, assert_layer_close, check_combine,
+                         check_selection,
                          e2e_selection_check, gpu_inputs, logit_bound, np_f, np_i, oracle_gates_from_logits,
                          out_tol, run_forward, run_staged, selection_scores)
 from oracle import moe_oracle as O
@@ -37,6 +38,10 @@ SMALL = {
                              bias_zipf_s=1.1),
     "softmax_bias_none": Workload("softmax_bias_none", T=333, d=128, N=32, F=128, k=3,
                                   norm="none", bias_zipf_s=1.1, bias_beta=0.05),
+    # >= 768 rows per expert: the grouped GEMM runs on CTA pairs (256-row tiles)
+    "pair_ragged": Workload("pair_ragged", T=1700, d=256, N=2, F=384, k=1),
+    "pair_shared_ragged_n": Workload("pair_shared_ragged_n", T=2100, d=192, N=2, F=320, k=1,
+                                     F_sh=256, score="sigmoid", bias_zipf_s=1.1),
 }
 
 
@@ -46,7 +51,8 @@ def oracle_inputs(inp):
 
 def reference_layer(w, o, idx_gpu):
     """Oracle layer output in fp64 with the GPU's (validated) selection:
-    gates from the oracle's own fp64 logits, experts and combine in fp64."""
+    gates from the oracle's own fp64 logits, experts and combine in fp64.
+    Also returns the magnitude |y_shared| + sum_j g_j |y_j| per element."""
     z = O.router_logits(o["h"], o["W_r"])
     p = O.scores(z, w.score)
     g = O.gates_from_scores(p, idx_gpu, w.norm)
@@ -55,7 +61,8 @@ def reference_layer(w, o, idx_gpu):
     ysh = None
     if w.F_sh > 0:
         ysh = O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"])
-    return O.combine(y_rows, inv, g, ysh), y_rows, ysh
+    mag = O.combine(np.abs(y_rows), inv, np.abs(g), None if ysh is None else np.abs(ysh))
+    return O.combine(y_rows, inv, g, ysh), mag
 
 
 @pytest.mark.parametrize("name", list(SMALL))
@@ -106,12 +113,12 @@ def test_small_workload_stagewise_parity(cuda_lib, name):
     check_combine(r, cfg, f"{name} combine")
 
     # ---- whole layer ----
-    out_ref, _, _ = reference_layer(w, o, idx)
-    assert_close_tol(np_f(r["out"]), out_ref, out_tol(w), f"{name} out")
+    out_ref, mag = reference_layer(w, o, idx)
+    assert_layer_close(np_f(r["out"]), out_ref, mag, out_tol(w), f"{name} out")
 
 
 @pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "tiny_fp32",
-                                  "many_experts"])
+                                  "many_experts", "pair_shared_ragged_n"])
 def test_forward_equals_stages_and_is_deterministic(cuda_lib, name):
     w = SMALL[name]
     cfg = api.config_for(w)

@@ -404,3 +404,57 @@ def test_mutation_dispatch_unstable_order(monkeypatch):
         inv = np.empty(T * k, dtype=np.int64); inv[order] = np.arange(T * k)
         return counts, offsets, t_flat[order], inv.reshape(T, k)
     _run_pins_expect_failure(monkeypatch, "dispatch", bad_dispatch, [test_page1_dispatch_table])
+
+
+# -------------------------------------------------------- routing statistics ---
+def test_stats_uniform_closed_forms():
+    """Equal logits and perfectly balanced assignments: L_bal = 1,
+    entropy = log N, z-loss = (z0 + log N)^2."""
+    T, N, k = 8, 4, 2
+    z0 = 0.7
+    z = np.full((T, N), z0)
+    S = np.array([[(t + j) % N for j in range(k)] for t in range(T)])
+    for score in (O.SOFTMAX, O.SIGMOID):
+        st = O.routing_stats(z, S, score, N)
+        assert abs(st["L_bal"] - 1.0) < 1e-12
+        assert abs(st["entropy"] - math.log(N)) < 1e-12
+        assert abs(st["L_z"] - (z0 + math.log(N)) ** 2) < 1e-12
+        np.testing.assert_allclose(st["P"], 1 / N, atol=1e-15)
+        np.testing.assert_allclose(st["f"], 1 / N, atol=1e-15)
+
+
+def test_stats_collapse_limit():
+    """Every token sent to expert 0 with probability -> 1: L_bal -> N, entropy -> 0."""
+    T, N = 5, 6
+    z = np.zeros((T, N)); z[:, 0] = 60.0
+    S = np.zeros((T, 1), dtype=np.int64)
+    st = O.routing_stats(z, S, O.SOFTMAX, N)
+    assert abs(st["L_bal"] - N) < 1e-12
+    assert st["entropy"] < 1e-20
+    assert abs(st["L_z"] - 60.0 ** 2) < 1e-9
+
+
+def test_stats_brute_force_and_library():
+    rng = np.random.default_rng(21)
+    T, N, k = 13, 5, 2
+    z = rng.standard_normal((T, N)) * 2
+    S, _, _, _ = O.route(z, k)
+    st = O.routing_stats(z, S, O.SOFTMAX, N)
+    # brute force, token by token with math
+    P = [0.0] * N; cnt = [0] * N; lz = 0.0; H = 0.0
+    for t in range(T):
+        ex = [math.exp(v) for v in z[t]]
+        tot = sum(ex)
+        lz += math.log(tot) ** 2
+        for i in range(N):
+            P[i] += ex[i] / tot / T
+            H -= ex[i] / tot * math.log(ex[i] / tot) / T
+        for j in range(k):
+            cnt[S[t, j]] += 1
+    f = [c / (T * k) for c in cnt]
+    assert abs(st["L_bal"] - N * sum(a * b for a, b in zip(f, P))) < 1e-12
+    assert abs(st["L_z"] - lz / T) < 1e-12
+    assert abs(st["entropy"] - H) < 1e-12
+    tz = torch.from_numpy(z)
+    np.testing.assert_allclose(O.logsumexp(z), torch.logsumexp(tz, -1).numpy(), atol=1e-13)
+    np.testing.assert_allclose(st["entropy"], torch.distributions.Categorical(logits=tz).entropy().mean().item(), atol=1e-12)

@@ -38,11 +38,15 @@ def _stale() -> bool:
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not verbose_ptxas and not _stale():
+def build(force: bool = False, verbose_ptxas: bool = False, out: str = LIB,
+          defines: tuple = ()) -> str:
+    """Compile the library to `out`; `defines` are extra -D tuning constants
+    (stage counts, CTA-pair threshold) for measurement builds."""
+    if not force and not verbose_ptxas and not defines and out == LIB and not _stale():
         return LIB
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I", os.path.join(ROOT, "include"), "-o", LIB + ".tmp"]
+           "-I", os.path.join(ROOT, "include"), "-o", out + ".tmp"]
+    cmd += [f"-D{d}" for d in defines]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     cmd += [os.path.join(CSRC, s) for s in SOURCES]
@@ -51,8 +55,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
     if verbose_ptxas:
         sys.stderr.write(res.stderr)
-    os.replace(LIB + ".tmp", LIB)
-    return LIB
+    os.replace(out + ".tmp", out)
+    return out
 
 
 if __name__ == "__main__":

@@ -44,8 +44,18 @@
 namespace moe {
 namespace {
 
+#ifndef MOE_GEMM_STAGES
+#define MOE_GEMM_STAGES 4
+#endif
+#ifndef MOE_PAIR_STAGES
+#define MOE_PAIR_STAGES 6
+#endif
+#ifndef MOE_PAIR_MIN_ROWS
+#define MOE_PAIR_MIN_ROWS 768
+#endif
+
 constexpr int kBM = 128;
-constexpr int kStages = 4;
+constexpr int kStages = MOE_GEMM_STAGES;
 constexpr int kThreads = 192;
 constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kTmemCols = 512;
@@ -56,6 +66,7 @@ constexpr uint32_t kStageB = 256 * 128;   // 256 rows x 128 B
 constexpr uint32_t kStageBytes = kStageA + kStageB;
 constexpr size_t kDynSmem = static_cast<size_t>(kStages) * kStageBytes + 1024;
 constexpr uint64_t kWaitBudgetNs = 4000000000ull;   // 4 s per wait
+constexpr int kPairMinRowsPerExpert = MOE_PAIR_MIN_ROWS;
 constexpr uint64_t kDrainBudgetNs = 200000000ull;   // 0.2 s
 
 enum { kSwiGLU = 0, kDown = 1, kRoute = 2 };
@@ -90,7 +101,7 @@ struct TileInfo {
   int g, m_blk, n_blk, row0, rows, ncols, b_row0, num_kb;
 };
 
-template <int BN, int BK>
+template <int BN, int BK, int BM = kBM>
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int* tile_start, const int* grp_off,
                                                 int G, const GemmParams& p) {
   int lo = 0, hi = G;  // tile_start[lo] <= tile < tile_start[hi]
@@ -113,9 +124,9 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int* tile_start,
     ti.b_row0 = 0;
     ti.num_kb = (p.K_shared + BK - 1) / BK;
   }
-  const int mt = (ti.rows + kBM - 1) / kBM;
+  const int mt = (ti.rows + BM - 1) / BM;
   const int nt = (ti.ncols + BN - 1) / BN;
-  const int nbands0 = (mt + kBandMax - 1) / kBandMax;
+  const int nbands0 = (mt + kBandMax * kBM / BM - 1) / (kBandMax * kBM / BM);
   const int band_sz = (mt + nbands0 - 1) / nbands0;
   const int l = tile - tile_start[lo];
   const int band = l / (band_sz * nt);
@@ -568,6 +579,281 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant (tcgen05.mma.cta_group::2): a cluster of two CTAs on two SMs
+// computes one 256-row tile. Each CTA loads its own 128 rows of A and one half
+// of the 256-row B tile (pass A: CTA 0 the W_gate rows, CTA 1 the W_up rows;
+// pass B: one 128-row half of W_down each), so each SM fetches 32 KB per
+// K-step instead of 48 KB for the same tensor-core work. The leader CTA (rank
+// 0) issues the MMAs for the pair; both CTAs' TMA loads count on the leader's
+// full barrier, the leader's commits arrive on both CTAs' empty and
+// accumulator-full barriers, and both CTAs' epilogue threads arrive on the
+// leader's accumulator-empty barrier. Each CTA drains its own 128 TMEM lanes.
+constexpr int kPairStages = MOE_PAIR_STAGES;
+constexpr uint32_t kPairStageA = 128 * 128;
+constexpr uint32_t kPairStageB = 128 * 128;
+constexpr uint32_t kPairStageBytes = kPairStageA + kPairStageB;
+constexpr size_t kPairDynSmem = static_cast<size_t>(kPairStages) * kPairStageBytes + 1024;
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA0,
+                             const __grid_constant__ CUtensorMap mapB0,
+                             const __grid_constant__ CUtensorMap mapB0u,
+                             const __grid_constant__ CUtensorMap mapA1,
+                             const __grid_constant__ CUtensorMap mapB1,
+                             const __grid_constant__ CUtensorMap mapB1u, const GemmParams p) {
+  using T = __nv_bfloat16;
+  constexpr int BK = 64;
+  constexpr int BM = 256;                                  // rows per pair tile
+  constexpr int BN = MODE == kSwiGLU ? 128 : 256;
+  const uint32_t idesc = make_idesc(BM, 256, 1u);
+
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full_bar[kPairStages];
+  __shared__ __align__(8) uint64_t empty_bar[kPairStages];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  __shared__ int tile_start[kMaxGroups + 1];
+  __shared__ int grp_off[kMaxGroups + 1];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int G = p.n_routed + (p.rows_shared > 0 ? 1 : 0);
+  volatile int* abort_v = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 256);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tmem_base_sh, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mapA0);
+      tma_prefetch_desc(&mapB0);
+      if (MODE == kSwiGLU) tma_prefetch_desc(&mapB0u);
+    }
+    for (int g = lane; g <= p.n_routed; g += 32) grp_off[g] = p.offsets[g];
+    __syncwarp();
+    bool bad = lane == 0 && (grp_off[0] != 0 || grp_off[p.n_routed] > p.rows_routed);
+    for (int g = lane; g < p.n_routed; g += 32) bad |= grp_off[g + 1] < grp_off[g];
+    bad = __any_sync(0xffffffffu, bad);
+    if (bad) {
+      if (lane == 0 && p.status != nullptr) atomicCAS(p.status, 0, MOE_ERR_DEVICE_CHECK);
+      for (int g = lane; g <= p.n_routed; g += 32) grp_off[g] = 0;
+      __syncwarp();
+    }
+    int carry = 0;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      int tiles = 0;
+      if (g < G) {
+        const int rows = g < p.n_routed ? grp_off[g + 1] - grp_off[g] : p.rows_shared;
+        const int ncols = g < p.n_routed ? p.n_out : p.n_out_shared;
+        tiles = ((rows + BM - 1) / BM) * ((ncols + BN - 1) / BN);
+      }
+      int incl = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < G) tile_start[g] = carry + incl - tiles;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[G] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+  const int total = tile_start[G];
+  const int cluster_id = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
+        const TileInfo ti = decode_tile<BN, BK, BM>(tile, tile_start, grp_off, G, p);
+        const bool dense = ti.g >= p.n_routed;
+        const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
+        const void* mB;
+        int b_row;
+        if (MODE == kSwiGLU) {
+          // CTA 0 holds the W_gate half of B, CTA 1 the W_up half
+          mB = leader ? (dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0))
+                      : (dense ? static_cast<const void*>(&mapB1u) : static_cast<const void*>(&mapB0u));
+          b_row = ti.b_row0 + ti.n_blk * BN;
+        } else {
+          mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
+          b_row = ti.b_row0 + ti.n_blk * BN + static_cast<int>(rank) * 128;
+        }
+        const int a_row = ti.row0 + ti.m_blk * BM + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
+          if (!mbar_wait_bounded_cluster(&empty_bar[stage], phase ^ 1u, abort_v, p.status,
+                                         p.budget_ns, MOE_ERR_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = smem + stage * kPairStageBytes;
+          uint8_t* sB = sA + kPairStageA;
+          const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
+          tma_load_2d_pair(sA, mA, full_leader, kb * BK, a_row);
+          tma_load_2d_pair(sB, mB, full_leader, kb * BK, b_row);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let loads already issued land before the CTA can leave
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA issuer (leader)
+    if (lane == 0 && leader) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
+        const TileInfo ti = decode_tile<BN, BK, BM>(tile, tile_start, grp_off, G, p);
+        if (!mbar_wait_bounded_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort_v, p.status,
+                                       p.budget_ns, MOE_ERR_TIMEOUT)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * kAccCols;
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
+          if (!mbar_wait_bounded_cluster(&full_bar[stage], phase, abort_v, p.status, p.budget_ns,
+                                         MOE_ERR_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * kPairStageBytes);
+          const uint32_t b_addr = a_addr + kPairStageA;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sw128_kmajor_desc(a_addr + kk * 32);
+            const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
+            mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit_pair(&empty_bar[stage], 0x3);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&tfull_bar[acc], 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // wait (bounded) for the MMAs already issued
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cluster_id; tile < total; tile += n_clusters) {
+      const TileInfo ti = decode_tile<BN, BK, BM>(tile, tile_start, grp_off, G, p);
+      if (!mbar_wait_bounded_cluster(&tfull_bar[acc], acc_phase, abort_v, p.status, p.budget_ns,
+                                     MOE_ERR_TIMEOUT))
+        break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(acc) * kAccCols;
+      const int row = ti.m_blk * BM + static_cast<int>(rank) * 128 + row_in_tile;
+      const bool row_ok = row < ti.rows;
+      const int col0 = ti.n_blk * BN;
+      const int cols_left = ti.ncols - col0;
+      const bool dense = ti.g >= p.n_routed;
+      T* out = dense ? static_cast<T*>(p.out_shared) + static_cast<size_t>(row) * p.n_out_shared
+                     : static_cast<T*>(p.out) + static_cast<size_t>(ti.row0 + row) * p.n_out;
+      out += col0;
+      if (MODE == kSwiGLU) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t gr[32], ur[32];
+          tmem_ld32_sync(tbase + c, gr);
+          tmem_ld32_sync(tbase + 128 + c, ur);
+          if (row_ok && c < cols_left) {
+            float act[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float gv = __uint_as_float(gr[i]);
+              const float uv = __uint_as_float(ur[i]);
+              act[i] = gv / (1.0f + __expf(-gv)) * uv;
+            }
+            store32(out + c, act, cols_left - c);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t v[32];
+          tmem_ld32_sync(tbase + c, v);
+          if (row_ok && c < cols_left) {
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+            store32(out + c, f, cols_left - c);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its peer may still signal its barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 // One CTA, one thread: waits on an mbarrier nothing arrives on, bounded.
 __global__ void selftest_wait_kernel(int32_t* status, uint64_t budget_ns) {
   __shared__ __align__(8) uint64_t bar;
@@ -624,10 +910,54 @@ cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid, 
 }
 
 int tiles_bound(int64_t rows_routed, int n_groups, int64_t n_out, int BN, int64_t rows_dense,
-                int64_t n_out_dense) {
-  int64_t b = (rows_routed / kBM + n_groups) * ((n_out + BN - 1) / BN);
-  if (rows_dense > 0) b += ((rows_dense + kBM - 1) / kBM) * ((n_out_dense + BN - 1) / BN);
+                int64_t n_out_dense, int BM = kBM) {
+  int64_t b = (rows_routed / BM + n_groups) * ((n_out + BN - 1) / BN);
+  if (rows_dense > 0) b += ((rows_dense + BM - 1) / BM) * ((n_out_dense + BN - 1) / BN);
   return static_cast<int>(b < 1 ? 1 : (b > (1 << 30) ? (1 << 30) : b));
+}
+
+// Clusters of two CTAs that can be resident at once (one CTA per SM).
+int pair_clusters(const void* kern, cudaLaunchConfig_t cfg) {
+  static int cache[64][2] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int slot = kern == reinterpret_cast<const void*>(grouped_gemm_pair_kernel<kSwiGLU>) ? 0 : 1;
+  if (dev >= 0 && dev < 64 && cache[dev][slot] > 0) return cache[dev][slot];
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = num_sms() / 2;
+  }
+  if (dev >= 0 && dev < 64) cache[dev][slot] = n;
+  return n;
+}
+
+template <int MODE>
+cudaError_t launch_gemm_pair(const CUtensorMap* maps, const GemmParams& p, int pair_tiles,
+                             cudaStream_t stream) {
+  auto kern = grouped_gemm_pair_kernel<MODE>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kPairDynSmem));
+  if (err != cudaSuccess) return err;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairDynSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  int clusters = pair_clusters(reinterpret_cast<const void*>(kern), cfg);
+  if (clusters > pair_tiles) clusters = pair_tiles;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  err = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -677,19 +1007,31 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   pa.out_shared = a.act_sh;
   pa.status = a.status;
   pa.budget_ns = kWaitBudgetNs;
-  int grid = tiles_bound(R, a.N, a.F, 128, sh ? a.T : 0, a.F_sh);
-  if (grid > sms) grid = sms;
-  cudaError_t err = a.dtype == MOE_F32 ? launch_gemm<kSwiGLU, float>(m, pa, grid, stream)
-                                       : launch_gemm<kSwiGLU, __nv_bfloat16>(m, pa, grid, stream);
+  // CTA pairs (256-row tiles) pay off when experts hold many rows on average;
+  // with few rows per expert the 128-row tiles waste less of the MMA.
+  const bool pair = a.dtype == MOE_BF16 && R >= static_cast<int64_t>(kPairMinRowsPerExpert) * a.N;
+  cudaError_t err;
+  if (pair) {
+    err = launch_gemm_pair<kSwiGLU>(m, pa, tiles_bound(R, a.N, a.F, 128, sh ? a.T : 0, a.F_sh, 256),
+                                    stream);
+  } else {
+    int grid = tiles_bound(R, a.N, a.F, 128, sh ? a.T : 0, a.F_sh);
+    if (grid > sms) grid = sms;
+    err = a.dtype == MOE_F32 ? launch_gemm<kSwiGLU, float>(m, pa, grid, stream)
+                             : launch_gemm<kSwiGLU, __nv_bfloat16>(m, pa, grid, stream);
+  }
   if (err != cudaSuccess) return err;
 
   // pass B: y = act Wd^T
   if (!make_map(&m[0], a.act, a.dtype, a.F, R, kBM)) return cudaErrorInvalidValue;
-  if (!make_map(&m[1], a.W_down, a.dtype, a.F, static_cast<uint64_t>(a.N) * a.d, 256)) return cudaErrorInvalidValue;
+  // a CTA pair splits the 256 B rows of a down tile 128/128 between its CTAs
+  const uint32_t down_box = pair ? 128 : 256;
+  if (!make_map(&m[1], a.W_down, a.dtype, a.F, static_cast<uint64_t>(a.N) * a.d, down_box))
+    return cudaErrorInvalidValue;
   m[2] = m[1];
   if (sh) {
     if (!make_map(&m[3], a.act_sh, a.dtype, a.F_sh, a.T, kBM)) return cudaErrorInvalidValue;
-    if (!make_map(&m[4], a.Ws_down, a.dtype, a.F_sh, a.d, 256)) return cudaErrorInvalidValue;
+    if (!make_map(&m[4], a.Ws_down, a.dtype, a.F_sh, a.d, down_box)) return cudaErrorInvalidValue;
     m[5] = m[4];
   } else {
     m[3] = m[0]; m[4] = m[1]; m[5] = m[1];
@@ -701,7 +1043,9 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   pb.n_out_shared = a.d;
   pb.out = a.y_rows;
   pb.out_shared = a.y_shared;
-  grid = tiles_bound(R, a.N, a.d, 256, sh ? a.T : 0, a.d);
+  if (pair) return launch_gemm_pair<kDown>(m, pb, tiles_bound(R, a.N, a.d, 256, sh ? a.T : 0, a.d, 256),
+                                           stream);
+  int grid = tiles_bound(R, a.N, a.d, 256, sh ? a.T : 0, a.d);
   if (grid > sms) grid = sms;
   return a.dtype == MOE_F32 ? launch_gemm<kDown, float>(m, pb, grid, stream)
                             : launch_gemm<kDown, __nv_bfloat16>(m, pb, grid, stream);
