@@ -198,6 +198,20 @@ moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r,
                        int32_t* counts, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
 
+/* Routing side statistics of one routing decision ([P1] §五 load-balancing
+ * loss and router z-loss; [P1] §十三 per-expert load and routing entropy).
+ *   logits [T, N] fp32 (moe_route's logits_out), idx [T, k] int32 (moe_route)
+ *   stats  [3 + 2N] fp32 out: L_bal, L_z, entropy, P_0..P_{N-1}, f_0..f_{N-1}
+ *          f_i = share of the T*k routed pairs sent to expert i;
+ *          P_i = mean over tokens of the router probability of expert i
+ *          (softmax; for a sigmoid router the scores divided by their sum);
+ *          L_bal = N * sum_i f_i P_i (1 when both are uniform);
+ *          L_z = mean over tokens of (log sum_i exp z_ti)^2;
+ *          entropy = mean over tokens of -sum_i p_ti log p_ti.
+ *   Deterministic (fixed summation order). ws: per-block partial sums. */
+moe_status moe_route_stats(const moe_config* cfg, const float* logits, const int32_t* idx,
+                           float* stats, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, copies the workspace's device status word into
  * *device_status (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK) and clears
  * it. Returns MOE_ERR_CUDA if the synchronisation or copy fails. */

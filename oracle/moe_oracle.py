@@ -377,3 +377,54 @@ def routing_stats(z, S, score_kind, N):
         plogp = np.where(p > 0, p * np.log(p), 0.0)
     return dict(L_bal=float(N * np.sum(f * P)), L_z=float(np.mean(logsumexp(z) ** 2)),
                 entropy=float(np.mean(-plogp.sum(axis=-1))), P=P, f=f)
+
+
+# --------------------------------------------------------------------------
+# Group-limited selection
+# --------------------------------------------------------------------------
+GROUP_MAX = "max"
+GROUP_TOPM_SUM = "topm_sum"
+
+
+def select_topk_grouped(q, k, n_group, topk_group, group_score=GROUP_MAX, top_m=2):
+    """Group-limited top-k ([P2] "跨设备时，为什么还要先选组？").
+
+    The N experts form n_group contiguous groups of N / n_group. Each group is
+    scored by its largest selection score (GROUP_MAX) or by the sum of its
+    top_m scores (GROUP_TOPM_SUM, the DeepSeek-V3 node score the page
+    describes); the topk_group best groups are kept (equal group scores: lower
+    group index first); the experts of every other group are masked with -inf
+    (not 0, so that negative scores cannot win through the mask); the top-k
+    then runs over the remaining experts with the usual order. Fewer than k
+    remaining candidates is an error, as on the page."""
+    q = np.asarray(q, dtype=np.float64)
+    T, N = q.shape
+    if n_group < 1 or N % n_group:
+        raise ValueError("N must split into n_group equal groups")
+    gs = N // n_group
+    if not 1 <= topk_group <= n_group:
+        raise ValueError("need 1 <= topk_group <= n_group")
+    if topk_group * gs < k:
+        raise ValueError("fewer candidates than k after group selection")
+    qg = q.reshape(T, n_group, gs)
+    if group_score == GROUP_MAX:
+        sg = qg.max(axis=-1)
+    elif group_score == GROUP_TOPM_SUM:
+        if not 1 <= top_m <= gs:
+            raise ValueError("need 1 <= top_m <= group size")
+        sg = -np.sort(-qg, axis=-1)[..., :top_m].sum(axis=-1)
+    else:
+        raise ValueError(f"unknown group score {group_score!r}")
+    kept = select_topk(sg, topk_group)
+    mask = np.full((T, n_group), -np.inf)
+    np.put_along_axis(mask, kept, 0.0, axis=-1)
+    return select_topk((qg + mask[..., None]).reshape(T, N), k)
+
+
+def route_grouped(z, k, n_group, topk_group, group_score=GROUP_MAX, top_m=2,
+                  score_kind=SOFTMAX, norm=NORM_SELECTED, sel_bias=None):
+    """route() with the selection limited to the best groups; gates as route()."""
+    p = scores(z, score_kind)
+    q = p if sel_bias is None else p + np.asarray(sel_bias, dtype=np.float64)[None, :]
+    S = select_topk_grouped(q, k, n_group, topk_group, group_score, top_m)
+    return S, gates_from_scores(p, S, norm), p, q

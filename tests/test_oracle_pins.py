@@ -458,3 +458,55 @@ def test_stats_brute_force_and_library():
     tz = torch.from_numpy(z)
     np.testing.assert_allclose(O.logsumexp(z), torch.logsumexp(tz, -1).numpy(), atol=1e-13)
     np.testing.assert_allclose(st["entropy"], torch.distributions.Categorical(logits=tz).entropy().mean().item(), atol=1e-12)
+
+
+# ------------------------------------------------------- group-limited top-k ---
+def test_page2_group_limited_example():
+    g = load_golden("page2_group_limited_example.json")
+    q = np.array([g["scores"]])
+    k = g["k"]
+    assert sorted(q[0, O.select_topk(q, k)[0]].tolist()) == sorted(g["unrestricted"])
+    Sm = O.select_topk_grouped(q, k, 2, 1, O.GROUP_MAX)
+    assert q[0, Sm[0]].tolist() == g["group_max_keep1"]
+    Ss = O.select_topk_grouped(q, k, 2, 1, O.GROUP_TOPM_SUM, top_m=2)
+    assert q[0, Ss[0]].tolist() == g["group_top2sum_keep1"]
+
+
+def test_grouped_special_cases_reduce_to_plain_topk():
+    rng = np.random.default_rng(31)
+    q = np.round(rng.standard_normal((40, 12)) * 2) / 2
+    for k in (1, 3, 5):
+        plain = O.select_topk(q, k)
+        # every group kept
+        np.testing.assert_array_equal(O.select_topk_grouped(q, k, 4, 4), plain)
+        # one expert per group, keep the k best groups
+        np.testing.assert_array_equal(O.select_topk_grouped(q, k, 12, k), plain)
+
+
+def test_grouped_masks_with_minus_infinity_not_zero():
+    q = np.array([[-5.0, -6.0, -1.0, -2.0]])
+    # group B (max -1) kept; group A must not win through a zero mask
+    assert O.select_topk_grouped(q, 2, 2, 1).tolist() == [[2, 3]]
+
+
+def test_grouped_brute_force_and_errors():
+    rng = np.random.default_rng(32)
+    for _ in range(100):
+        G = int(rng.integers(1, 5)); gs = int(rng.integers(1, 4)); N = G * gs
+        kg = int(rng.integers(1, G + 1))
+        k = int(rng.integers(1, kg * gs + 1))
+        m = int(rng.integers(1, gs + 1))
+        q = np.round(rng.standard_normal(N) * 2) / 2
+        for rule in (O.GROUP_MAX, O.GROUP_TOPM_SUM):
+            got = O.select_topk_grouped(q[None], k, G, kg, rule, m)[0].tolist()
+            # brute force: group scores, rank-count the groups, then rank-count experts
+            def gscore(gi):
+                vals = sorted(q[gi * gs:(gi + 1) * gs], reverse=True)
+                return vals[0] if rule == O.GROUP_MAX else sum(vals[:m])
+            kept = set(O.topk_by_rank_count([gscore(gi) for gi in range(G)], kg))
+            cand = [float(q[i]) if i // gs in kept else -np.inf for i in range(N)]
+            assert got == O.topk_by_rank_count(cand, k)
+    with pytest.raises(ValueError):
+        O.select_topk_grouped(np.zeros((1, 8)), 5, 4, 2)      # 2 groups x 2 = 4 < 5
+    with pytest.raises(ValueError):
+        O.select_topk_grouped(np.zeros((1, 9)), 2, 4, 2)      # 9 experts, 4 groups

@@ -32,7 +32,7 @@ NORMS = {"selected": 0, "none": 1}
 ENTRY_POINTS = (
     "moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
     "moe_forward", "moe_read_status", "moe_selftest_wait_timeout", "moe_status_string",
-    "moe_dispatch_noalloc",
+    "moe_dispatch_noalloc", "moe_route_stats",
 )
 
 
@@ -67,6 +67,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_route.argtypes = [cfgp] + [_vp] * 8 + [_vp, _sz, _vp]
     lib.moe_dispatch.argtypes = [cfgp] + [_vp] * 7 + [_vp, _sz, _vp]
     lib.moe_dispatch_noalloc.argtypes = [cfgp] + [_vp] * 7 + [_vp]
+    lib.moe_route_stats.argtypes = [cfgp] + [_vp] * 3 + [_vp, _sz, _vp]
     lib.moe_expert_ffn.argtypes = [cfgp] + [_vp] * 11 + [_vp, _sz, _vp]
     lib.moe_combine.argtypes = [cfgp] + [_vp] * 5 + [_vp]
     lib.moe_forward.argtypes = [cfgp] + [_vp] * 15 + [_vp, _sz, _vp]
@@ -173,6 +174,13 @@ def moe_forward(cfg, h, W_r, b_r, sel_bias, W_gate, W_up, W_down, Ws_gate, Ws_up
                            _p(logits_out), _p(idx), _p(gate), _p(counts), _p(ws), ws.numel(),
                            _stream(stream))
     _check(s, "moe_forward")
+
+
+def moe_route_stats(cfg, logits, idx, stats, ws, stream=None):
+    """stats [3 + 2N] fp32: L_bal, L_z, entropy, P[N], f[N]."""
+    s = load().moe_route_stats(ctypes.byref(cfg), _p(logits), _p(idx), _p(stats), _p(ws),
+                               ws.numel(), _stream(stream))
+    _check(s, "moe_route_stats")
 
 
 def read_status(ws: torch.Tensor, stream=None) -> int:

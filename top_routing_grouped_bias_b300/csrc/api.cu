@@ -201,6 +201,19 @@ moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r, co
   return combine_impl(cfg, y_rows, inv, gate, y_sh, out, stream);
 }
 
+moe_status moe_route_stats(const moe_config* cfg, const float* logits, const int32_t* idx,
+                           float* stats, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!ok_f32(logits) || !ok_f32(idx) || !ok_f32(stats)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  if (!ws_ok(ws, ws_bytes, L.end_dispatch)) return MOE_ERR_WORKSPACE;
+  StatsArgs a{};
+  a.logits = logits; a.idx = idx; a.out = stats; a.partial = at<float>(ws, L.stats);
+  a.T = cfg->T; a.N = cfg->N; a.k = cfg->k; a.score = cfg->score;
+  return from_cuda(launch_route_stats(a, stream));
+}
+
 moe_status moe_read_status(void* ws, size_t ws_bytes, int32_t* device_status, cudaStream_t stream) {
   if (ws == nullptr || ws_bytes < 256 || device_status == nullptr) return MOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;

@@ -21,7 +21,8 @@ inline int elem_size(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 // points use the prefixes they need: dispatch [status, block_base],
 // expert FFN [status .. act_sh], forward everything.
 struct WsLayout {
-  size_t status, block_base, act, act_sh, offsets, counts, row_token, inv, x_disp, y_rows, y_sh;
+  size_t status, block_base, stats, act, act_sh, offsets, counts, row_token, inv, x_disp, y_rows,
+      y_sh;
   size_t end_dispatch, end_ffn, total;
 };
 
@@ -38,6 +39,7 @@ inline WsLayout ws_layout(const moe_config& c) {
   };
   L.status = take(256);
   L.block_base = take(nb * static_cast<size_t>(c.N) * 4);
+  L.stats = take(nb * (2 * static_cast<size_t>(c.N) + 2) * 4);
   L.end_dispatch = o;
   L.act = take(R * static_cast<size_t>(c.ffn) * e);
   L.act_sh = take(T * static_cast<size_t>(c.ffn_shared) * e);
@@ -120,6 +122,17 @@ struct CombineArgs {
   int32_t d, k, dtype;
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+
+// ---- routing side statistics ----
+struct StatsArgs {
+  const float* logits;  // [T, N]
+  const int32_t* idx;   // [T, k]
+  float* out;           // [3 + 2N]
+  float* partial;       // scratch [nb][2N + 2]
+  int64_t T;
+  int32_t N, k, score;
+};
+cudaError_t launch_route_stats(const StatsArgs& a, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t budget_ns, cudaStream_t stream);
 

@@ -1,0 +1,168 @@
+// Routing side statistics of one routing decision.
+//
+// Pages: "MOE 专家选择与路由机制" §五 (load-balancing loss N * sum_i f_i P_i with
+// f_i the share of assignments to expert i and P_i its mean router
+// probability; router z-loss, the mean squared log-sum-exp of the logits) and
+// §十三 (per-expert load and routing entropy are the quantities to monitor).
+//
+// Router probabilities are softmax(z) for a softmax router and the sigmoid
+// scores divided by their per-token sum for a sigmoid router.
+//
+// Two launches, deterministic (fixed summation order, integer counts):
+//   partial  one block per 256 tokens: per-token max / normaliser / lse^2 /
+//            entropy (warp per token), then per-expert probability sums in
+//            token order and assignment counts
+//   final    one block: sums the block partials in block order and writes
+//            [L_bal, L_z, entropy, P_0..P_{N-1}, f_0..f_{N-1}]
+#include <math.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTok = kDispatchTokensPerBlock;  // 256 tokens per block
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
+  __shared__ float s_m[kTok], s_norm[kTok], s_lse2[kTok], s_ent[kTok];
+  extern __shared__ int s_cnt[];  // [N]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N;
+  const bool softmax = a.score == MOE_SCORE_SOFTMAX;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTok;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) s_cnt[e] = 0;
+  for (int lt = warp; lt < kTok; lt += 8) {
+    const int64_t t = t0 + lt;
+    if (t >= a.T) {
+      if (lane == 0) { s_m[lt] = 0.f; s_norm[lt] = 1.f; s_lse2[lt] = 0.f; s_ent[lt] = 0.f; }
+      continue;
+    }
+    const float* z = a.logits + t * N;
+    float m = -INFINITY;
+    for (int e = lane; e < N; e += 32) m = fmaxf(m, z[e]);
+    m = warp_max_f(m);
+    float se = 0.f, sze = 0.f, ssig = 0.f;
+    for (int e = lane; e < N; e += 32) {
+      const float ex = expf(z[e] - m);
+      se += ex;
+      sze += ex * (z[e] - m);
+      if (!softmax) ssig += 1.f / (1.f + expf(-z[e]));
+    }
+    se = warp_sum_f(se);
+    sze = warp_sum_f(sze);
+    const float lse = m + logf(se);
+    float norm, ent;
+    if (softmax) {
+      norm = se;
+      ent = logf(se) - sze / se;  // -sum p log p with log p = z - m - log(se)
+    } else {
+      norm = warp_sum_f(ssig);
+      float h = 0.f;
+      for (int e = lane; e < N; e += 32) {
+        const float p = 1.f / (1.f + expf(-z[e])) / norm;
+        if (p > 0.f) h -= p * logf(p);
+      }
+      ent = warp_sum_f(h);
+    }
+    if (lane == 0) {
+      s_m[lt] = m;
+      s_norm[lt] = norm;
+      s_lse2[lt] = lse * lse;
+      s_ent[lt] = ent;
+    }
+  }
+  __syncthreads();
+  // assignment counts (integers: order-independent)
+  for (int i = threadIdx.x; i < kTok * a.k; i += blockDim.x) {
+    const int64_t t = t0 + i / a.k;
+    if (t < a.T) {
+      const int e = a.idx[t0 * a.k + i];
+      if (e >= 0 && e < N) atomicAdd(&s_cnt[e], 1);
+    }
+  }
+  __syncthreads();
+  float* P = a.partial + static_cast<size_t>(blockIdx.x) * (2 * N + 2);
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    float acc = 0.f;
+    for (int lt = 0; lt < kTok; ++lt) {
+      const int64_t t = t0 + lt;
+      if (t >= a.T) break;
+      const float z = a.logits[t * N + e];
+      acc += softmax ? expf(z - s_m[lt]) / s_norm[lt] : 1.f / (1.f + expf(-z)) / s_norm[lt];
+    }
+    P[e] = acc;
+    P[N + e] = static_cast<float>(s_cnt[e]);
+  }
+  if (threadIdx.x == 0) {
+    float l2 = 0.f, en = 0.f;
+    for (int lt = 0; lt < kTok; ++lt) {
+      l2 += s_lse2[lt];
+      en += s_ent[lt];
+    }
+    P[2 * N] = l2;
+    P[2 * N + 1] = en;
+  }
+}
+
+__global__ void __launch_bounds__(1024) stats_final_kernel(StatsArgs a, int nb) {
+  __shared__ float red[32];
+  const int N = a.N;
+  const float invT = 1.f / static_cast<float>(a.T);
+  const float invTk = 1.f / (static_cast<float>(a.T) * static_cast<float>(a.k));
+  float local = 0.f;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    float ps = 0.f, cs = 0.f;
+    for (int b = 0; b < nb; ++b) {
+      const float* P = a.partial + static_cast<size_t>(b) * (2 * N + 2);
+      ps += P[e];
+      cs += P[N + e];
+    }
+    const float Pe = ps * invT, fe = cs * invTk;
+    a.out[3 + e] = Pe;
+    a.out[3 + N + e] = fe;
+    local += fe * Pe;
+  }
+  // block reduction in a fixed tree order
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  local = warp_sum_f(local);
+  if (lane == 0) red[w] = local;
+  __syncthreads();
+  if (w == 0) {
+    float v = lane < (blockDim.x >> 5) ? red[lane] : 0.f;
+    v = warp_sum_f(v);
+    if (lane == 0) {
+      float l2 = 0.f, en = 0.f;
+      for (int b = 0; b < nb; ++b) {
+        const float* P = a.partial + static_cast<size_t>(b) * (2 * N + 2);
+        l2 += P[2 * N];
+        en += P[2 * N + 1];
+      }
+      a.out[0] = static_cast<float>(N) * v;
+      a.out[1] = l2 * invT;
+      a.out[2] = en * invT;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_stats(const StatsArgs& a, cudaStream_t stream) {
+  if (a.T == 0) return cudaMemsetAsync(a.out, 0, sizeof(float) * (3 + 2 * a.N), stream);
+  const int nb = static_cast<int>((a.T + kTok - 1) / kTok);
+  stats_partial_kernel<<<nb, 256, a.N * sizeof(int), stream>>>(a);
+  stats_final_kernel<<<1, 1024, 0, stream>>>(a, nb);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
