@@ -198,6 +198,29 @@ moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r,
                        int32_t* counts, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
 
+/* Group-limited selection ([P2] 跨设备时，为什么还要先选组？): the N experts form
+ * n_group contiguous groups of N / n_group; each group is scored by its
+ * largest selection score (rule 0) or the sum of its top_m scores (rule 1);
+ * the topk_group best groups are kept (equal scores: lower group index); the
+ * other groups' experts are masked with -inf and the top-k runs over the rest. */
+typedef struct {
+  int32_t n_group;     /* 1..32, divides N */
+  int32_t topk_group;  /* 1..n_group; topk_group * N / n_group >= k ("too few candidates") */
+  int32_t rule;        /* 0 = group max, 1 = sum of the group's top_m scores */
+  int32_t top_m;       /* 1..min(8, N / n_group), used by rule 1 */
+} moe_group_config;
+
+/* moe_route with group-limited selection; arguments as moe_route plus `grp`.
+ * Scores, bias and gates are as in moe_route (gates from the un-biased scores
+ * of the selected experts). Invalid group settings, including fewer than k
+ * candidates in the kept groups, return MOE_ERR_INVALID_ARG. Routing from h
+ * needs the workspace (moe_workspace_size) for the logits when logits_out is
+ * NULL. */
+moe_status moe_route_grouped(const moe_config* cfg, const moe_group_config* grp, const void* h,
+                             const void* W_r, const float* b_r, const float* sel_bias,
+                             const float* logits_in, float* logits_out, int32_t* idx,
+                             float* gate, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Routing side statistics of one routing decision ([P1] §五 load-balancing
  * loss and router z-loss; [P1] §十三 per-expert load and routing entropy).
  *   logits [T, N] fp32 (moe_route's logits_out), idx [T, k] int32 (moe_route)

@@ -75,3 +75,79 @@ def test_route_stats_full_size(cuda_lib, name):
     ref = O.routing_stats(np_f(logits), np_i(idx), w.score, w.N)
     _check_stats(got, ref, w.N)
     print(f"{name}: L_bal {got[0]:.4f} L_z {got[1]:.4f} entropy {got[2]:.4f}")
+
+
+# ------------------------------------------------------- group-limited top-k ---
+def _route_grouped(cfg, grp, z=None, h=None, W_r=None, bias=None):
+    dev = "cuda"
+    ws = api.alloc_workspace(cfg, dev)
+    logits = torch.empty((cfg.T, cfg.N), dtype=torch.float32, device=dev)
+    idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    gate = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+    api.moe_route_grouped(cfg, grp, h, W_r, None, None if bias is None else bias.to(dev),
+                          None if z is None else z.to(dev), logits, idx, gate, ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    return logits, idx, gate
+
+
+def test_grouped_page2_example(cuda_lib):
+    """Scores [0.90, 0.10 | 0.80, 0.79] as sigmoid scores: group max keeps A,
+    the top-2 sum keeps B (1.59 > 1.00)."""
+    from conftest import load_golden
+    g = load_golden("page2_group_limited_example.json")
+    q = torch.tensor([g["scores"]], dtype=torch.float64)
+    z = torch.log(q / (1 - q)).to(torch.float32)
+    cfg = api.make_config(1, 8, 4, 2, 8, score="sigmoid")
+    _, idx, _ = _route_grouped(cfg, api.make_group_config(2, 1, "max"), z=z)
+    assert np_i(idx)[0].tolist() == [0, 1]
+    _, idx, _ = _route_grouped(cfg, api.make_group_config(2, 1, "topm_sum", 2), z=z)
+    assert np_i(idx)[0].tolist() == [2, 3]
+    _, idx, _ = _route_grouped(cfg, api.make_group_config(2, 2, "max"), z=z)
+    assert np_i(idx)[0].tolist() == [0, 2]
+
+
+@pytest.mark.parametrize("N,k,G,kg,rule,m,score", [
+    (64, 8, 8, 4, "topm_sum", 2, "sigmoid"), (64, 6, 8, 3, "max", 1, "softmax"),
+    (256, 8, 8, 4, "topm_sum", 2, "sigmoid"), (32, 4, 32, 4, "max", 1, "softmax"),
+    (60, 5, 6, 2, "topm_sum", 3, "softmax")])
+def test_grouped_given_logits_exact(cuda_lib, N, k, G, kg, rule, m, score):
+    T = 700
+    z = synth.random_logits(T, N, seed=N * G + k, std=1.5, ties=True)
+    cfg = api.make_config(T, 8, N, k, 8, score=score)
+    _, idx, gate = _route_grouped(cfg, api.make_group_config(G, kg, rule, m), z=z)
+    rule_o = O.GROUP_MAX if rule == "max" else O.GROUP_TOPM_SUM
+    S, g, _, _ = O.route_grouped(to_f64(z), k, G, kg, rule_o, m, score, "selected")
+    assert (np_i(idx) == S).all()
+    np.testing.assert_allclose(np_f(gate), g, atol=1e-6, rtol=0)
+
+
+def test_grouped_from_hidden_states_with_bias(cuda_lib):
+    """bf16 routing from h: logits on the tensor cores, then the grouped
+    selection (DeepSeek-V3-like: 8 groups, keep 4, top-2 sums, sigmoid + bias)."""
+    w = Workload("grouped", T=500, d=256, N=64, F=64, k=8, score="sigmoid", bias_zipf_s=1.1,
+                 bias_beta=0.3)
+    cfg = api.config_for(w)
+    inp = synth.make_inputs(w, seed=2, device="cuda")
+    logits, idx, gate = _route_grouped(cfg, api.make_group_config(8, 4, "topm_sum", 2),
+                                       h=inp["h"], W_r=inp["W_r"], bias=inp["sel_bias"])
+    z = np_f(logits)
+    from gpu_helpers import logit_bound
+    assert (np.abs(z - O.router_logits(to_f64(inp["h"]), to_f64(inp["W_r"])))
+            <= logit_bound(to_f64(inp["h"]), to_f64(inp["W_r"]))).all()
+    S, g, _, _ = O.route_grouped(z, w.k, 8, 4, O.GROUP_TOPM_SUM, 2, w.score, w.norm,
+                                 to_f64(inp["sel_bias"]))
+    same = (np_i(idx) == S).all(axis=1)
+    # fp32 group sums and scores may flip near-ties; everything else is exact
+    assert same.mean() >= 0.99, same.mean()
+    np.testing.assert_allclose(np_f(gate)[same], g[same], atol=1e-6, rtol=0)
+
+
+def test_grouped_rejects_too_few_candidates(cuda_lib):
+    import ctypes
+    lib = api.load()
+    fake = ctypes.c_void_p(1 << 20)
+    cfg = api.make_config(16, 8, 8, 5, 8)
+    grp = api.make_group_config(4, 2, "max")          # 2 groups x 2 experts = 4 < 5
+    assert lib.moe_route_grouped(ctypes.byref(cfg), ctypes.byref(grp), None, None, None, None,
+                                 fake, None, fake, fake, None, 0, None) == api.MOE_ERR_INVALID_ARG

@@ -32,7 +32,7 @@ NORMS = {"selected": 0, "none": 1}
 ENTRY_POINTS = (
     "moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
     "moe_forward", "moe_read_status", "moe_selftest_wait_timeout", "moe_status_string",
-    "moe_dispatch_noalloc", "moe_route_stats",
+    "moe_dispatch_noalloc", "moe_route_stats", "moe_route_grouped",
 )
 
 
@@ -40,6 +40,19 @@ class MoeError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__(f"{where} failed: {status_string(status)} ({status})")
+
+
+class MoeGroupConfig(ctypes.Structure):
+    _fields_ = [("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
+                ("rule", ctypes.c_int32), ("top_m", ctypes.c_int32)]
+
+
+GROUP_RULES = {"max": 0, "topm_sum": 1}
+
+
+def make_group_config(n_group: int, topk_group: int, rule: str = "max",
+                      top_m: int = 2) -> MoeGroupConfig:
+    return MoeGroupConfig(int(n_group), int(topk_group), GROUP_RULES[rule], int(top_m))
 
 
 class MoeConfig(ctypes.Structure):
@@ -68,6 +81,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_dispatch.argtypes = [cfgp] + [_vp] * 7 + [_vp, _sz, _vp]
     lib.moe_dispatch_noalloc.argtypes = [cfgp] + [_vp] * 7 + [_vp]
     lib.moe_route_stats.argtypes = [cfgp] + [_vp] * 3 + [_vp, _sz, _vp]
+    lib.moe_route_grouped.argtypes = [cfgp, ctypes.POINTER(MoeGroupConfig)] + [_vp] * 8 + \
+        [_vp, _sz, _vp]
     lib.moe_expert_ffn.argtypes = [cfgp] + [_vp] * 11 + [_vp, _sz, _vp]
     lib.moe_combine.argtypes = [cfgp] + [_vp] * 5 + [_vp]
     lib.moe_forward.argtypes = [cfgp] + [_vp] * 15 + [_vp, _sz, _vp]
@@ -174,6 +189,14 @@ def moe_forward(cfg, h, W_r, b_r, sel_bias, W_gate, W_up, W_down, Ws_gate, Ws_up
                            _p(logits_out), _p(idx), _p(gate), _p(counts), _p(ws), ws.numel(),
                            _stream(stream))
     _check(s, "moe_forward")
+
+
+def moe_route_grouped(cfg, grp, h, W_r, b_r, sel_bias, logits_in, logits_out, idx, gate,
+                      ws=None, stream=None):
+    s = load().moe_route_grouped(ctypes.byref(cfg), ctypes.byref(grp), _p(h), _p(W_r), _p(b_r),
+                                 _p(sel_bias), _p(logits_in), _p(logits_out), _p(idx), _p(gate),
+                                 _p(ws), 0 if ws is None else ws.numel(), _stream(stream))
+    _check(s, "moe_route_grouped")
 
 
 def moe_route_stats(cfg, logits, idx, stats, ws, stream=None):

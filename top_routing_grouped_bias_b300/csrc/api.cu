@@ -201,6 +201,58 @@ moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r, co
   return combine_impl(cfg, y_rows, inv, gate, y_sh, out, stream);
 }
 
+moe_status moe_route_grouped(const moe_config* cfg, const moe_group_config* grp, const void* h,
+                             const void* W_r, const float* b_r, const float* sel_bias,
+                             const float* logits_in, float* logits_out, int32_t* idx,
+                             float* gate, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (grp == nullptr) return MOE_ERR_INVALID_ARG;
+  const int N = cfg->N;
+  if (grp->n_group < 1 || grp->n_group > 32 || N % grp->n_group != 0) return MOE_ERR_INVALID_ARG;
+  const int gs = N / grp->n_group;
+  if (grp->topk_group < 1 || grp->topk_group > grp->n_group) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(grp->topk_group) * gs < cfg->k) return MOE_ERR_INVALID_ARG;
+  if (grp->rule != 0 && grp->rule != 1) return MOE_ERR_INVALID_ARG;
+  if (grp->rule == 1 && (grp->top_m < 1 || grp->top_m > 8 || grp->top_m > gs))
+    return MOE_ERR_INVALID_ARG;
+  if (!ok_f32(idx) || !ok_f32(gate) || !ok_opt_f32(b_r) || !ok_opt_f32(sel_bias) ||
+      !ok_opt_f32(logits_out))
+    return MOE_ERR_INVALID_ARG;
+  if (h != nullptr ? (!ok_tensor(h) || !ok_tensor(W_r)) : !ok_f32(logits_in))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  RouteArgs a{};
+  a.h = h; a.W_r = W_r; a.b_r = b_r; a.sel_bias = sel_bias; a.logits_in = logits_in;
+  a.logits_out = logits_out; a.idx = idx; a.gate = gate; a.T = cfg->T; a.d = cfg->d;
+  a.N = N; a.k = cfg->k; a.score = cfg->score; a.norm = cfg->norm; a.dtype = cfg->dtype;
+  a.n_group = grp->n_group; a.topk_group = grp->topk_group; a.group_rule = grp->rule;
+  a.top_m = grp->top_m;
+  int32_t* status = (ws != nullptr && ws_bytes >= 256 && aligned(ws, 256))
+                        ? static_cast<int32_t*>(ws) : nullptr;
+  a.status = status;
+  if (h != nullptr && cfg->dtype == MOE_BF16 && N <= 256 && a.n_group > 1) {
+    // logits on the tensor cores, then the grouped selection from them
+    float* z = logits_out;
+    if (z == nullptr) {
+      const WsLayout L = ws_layout(*cfg);
+      if (!ws_ok(ws, ws_bytes, L.total)) return MOE_ERR_WORKSPACE;
+      z = at<float>(ws, L.logits);
+    }
+    RouteArgs t = a;
+    t.n_group = 1;
+    t.logits_out = z;
+    s = from_cuda(launch_route(t, stream));
+    if (s != MOE_OK) return s;
+    a.h = nullptr;
+    a.W_r = nullptr;
+    a.b_r = nullptr;  // already inside z
+    a.logits_in = z;
+    a.logits_out = nullptr;
+  }
+  return from_cuda(launch_route(a, stream));
+}
+
 moe_status moe_route_stats(const moe_config* cfg, const float* logits, const int32_t* idx,
                            float* stats, void* ws, size_t ws_bytes, cudaStream_t stream) {
   moe_status s = check_config(cfg);

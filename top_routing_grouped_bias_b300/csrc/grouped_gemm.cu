@@ -1052,7 +1052,7 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
 }
 
 bool route_on_tensor_cores(const RouteArgs& a) {
-  return a.h != nullptr && a.dtype == MOE_BF16 && a.N <= 256;
+  return a.h != nullptr && a.dtype == MOE_BF16 && a.N <= 256 && a.n_group <= 1;
 }
 
 cudaError_t launch_route_mma(const RouteArgs& a, cudaStream_t stream) {

@@ -22,7 +22,7 @@ inline int elem_size(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 // expert FFN [status .. act_sh], forward everything.
 struct WsLayout {
   size_t status, block_base, stats, act, act_sh, offsets, counts, row_token, inv, x_disp, y_rows,
-      y_sh;
+      y_sh, logits;
   size_t end_dispatch, end_ffn, total;
 };
 
@@ -51,6 +51,7 @@ inline WsLayout ws_layout(const moe_config& c) {
   L.x_disp = take(R * static_cast<size_t>(c.d) * e);
   L.y_rows = take(R * static_cast<size_t>(c.d) * e);
   L.y_sh = take(c.ffn_shared > 0 ? T * static_cast<size_t>(c.d) * e : 0);
+  L.logits = take(T * static_cast<size_t>(c.N) * 4);
   L.total = o;
   return L;
 }
@@ -68,6 +69,8 @@ struct RouteArgs {
   int32_t* status;  // device status word or null
   int64_t T;
   int32_t d, N, k, score, norm, dtype;
+  // group-limited selection (n_group <= 1: off)
+  int32_t n_group, topk_group, group_rule, top_m;
 };
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 // Router as a tcgen05 GEMM with a top-k epilogue (bf16, N <= 256, from h).

@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
   if (t >= a.T) return;
   const int N = a.N, k = a.k;
   const bool has_bias = a.sel_bias != nullptr;
-  float* z = route_smem + static_cast<size_t>(warp) * N * (has_bias ? 2 : 1);
+  float* z = route_smem + static_cast<size_t>(warp) * N * ((has_bias || a.n_group > 1) ? 2 : 1);
   float* q = z + N;
 
   // ---- logits ----
@@ -123,14 +123,66 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
   }
 
   // ---- selection score ----
+  // with group-limited selection the group scores are sums/maxima of the
+  // scores themselves, so q = p (+ bias) is formed even without a bias
+  const bool grouped = a.n_group > 1;
   const float* sel = z;
-  if (has_bias) {
+  if (has_bias || grouped) {
     for (int e = lane; e < N; e += 32) {
       const float p = a.score == MOE_SCORE_SOFTMAX ? expf(z[e] - m) / s : 1.f / (1.f + expf(-z[e]));
-      q[e] = p + a.sel_bias[e];
+      q[e] = p + (has_bias ? a.sel_bias[e] : 0.f);
     }
     __syncwarp();
     sel = q;
+  }
+
+  // ---- group-limited selection: keep the topk_group best groups ----
+  uint32_t gkeep = 0xffffffffu;
+  int gs = N;
+  if (grouped) {
+    gs = N / a.n_group;
+    float gscore = -INFINITY;
+    if (lane < a.n_group) {
+      const float* sg = sel + lane * gs;
+      if (a.group_rule == 0) {
+        for (int i = 0; i < gs; ++i) gscore = fmaxf(gscore, sg[i]);
+      } else {
+        float tv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) tv[j] = -INFINITY;
+        for (int i = 0; i < gs; ++i) {
+          float v = sg[i];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j < a.top_m && v > tv[j]) {
+              const float t = tv[j];
+              tv[j] = v;
+              v = t;
+            }
+          }
+        }
+        gscore = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < a.top_m) gscore += tv[j];
+      }
+    }
+    gkeep = 0;
+    for (int r = 0; r < a.topk_group; ++r) {
+      const bool cand = lane < a.n_group && !((gkeep >> lane) & 1u);
+      float best = cand ? gscore : -INFINITY;
+      int best_g = cand ? lane : 0x7fffffff;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int og = __shfl_xor_sync(0xffffffffu, best_g, o);
+        if (ov > best || (ov == best && og < best_g)) {
+          best = ov;
+          best_g = og;
+        }
+      }
+      if (best_g < 32) gkeep |= 1u << best_g;
+    }
   }
 
   // ---- top-k: k rounds of a warp arg-max, lowest index on ties ----
@@ -141,6 +193,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
     int best_e = 0x7fffffff;
     for (int i = 0, e = lane; e < N; ++i, e += 32) {
       if ((taken >> i) & 1u) continue;
+      if (!((gkeep >> (e / gs)) & 1u)) continue;  // masked group (-inf)
       const float v = sel[e];
       if (v > best || (v == best && e < best_e)) {
         best = v;
@@ -194,7 +247,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
   if (route_on_tensor_cores(a)) return launch_route_mma(a, stream);
-  const size_t smem = static_cast<size_t>(kRouteWarps) * a.N * (a.sel_bias ? 2 : 1) * sizeof(float);
+  const bool two = a.sel_bias != nullptr || a.n_group > 1;
+  const size_t smem = static_cast<size_t>(kRouteWarps) * a.N * (two ? 2 : 1) * sizeof(float);
   const unsigned grid = static_cast<unsigned>((a.T + kRouteWarps - 1) / kRouteWarps);
   cudaError_t err;
   if (a.dtype == MOE_F32) {
