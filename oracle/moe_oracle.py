@@ -428,3 +428,57 @@ def route_grouped(z, k, n_group, topk_group, group_score=GROUP_MAX, top_m=2,
     q = p if sel_bias is None else p + np.asarray(sel_bias, dtype=np.float64)[None, :]
     S = select_topk_grouped(q, k, n_group, topk_group, group_score, top_m)
     return S, gates_from_scores(p, S, norm), p, q
+
+
+# --------------------------------------------------------------------------
+# Expert capacity and token dropping
+# --------------------------------------------------------------------------
+def expert_capacity(T, k, N, capacity_factor):
+    """C = ceil(capacity_factor * T * k / N) ([P1] §六 Expert Capacity)."""
+    import math
+    return int(math.ceil(capacity_factor * T * k / N))
+
+
+def dispatch_capacity(S, N, C):
+    """Dispatch with at most C rows per expert ([P1] §六: tokens beyond the
+    capacity may be dropped; the page leaves the policy to the
+    implementation). Reading taken: each expert keeps its first C (token,
+    slot) pairs in token order and drops the rest; a dropped pair has
+    inv = -1 and contributes nothing (the token keeps its other experts and
+    the residual path); gates are not renormalised.
+    Returns counts (kept rows per expert), offsets, row_token (kept rows
+    only), inv [T,k] with -1 for dropped pairs."""
+    S = np.asarray(S)
+    T, k = S.shape
+    full_counts, full_offsets, full_row_token, full_inv = dispatch(S, N)
+    counts = np.minimum(full_counts, C)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    inv = np.full((T, k), -1, dtype=np.int64)
+    row_token = np.empty(int(counts.sum()), dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(S[t, j])
+            rank = int(full_inv[t, j] - full_offsets[e])   # position among e's pairs
+            if rank < C:
+                inv[t, j] = offsets[e] + rank
+                row_token[offsets[e] + rank] = t
+    return counts, offsets, row_token, inv
+
+
+def moe_forward_capacity(h, W_r, W_gate, W_up, W_down, k, C, score_kind=SOFTMAX,
+                         norm=NORM_SELECTED, sel_bias=None, b_r=None, shared=None):
+    """The layer with expert capacity C: route, dispatch_capacity, experts on
+    the kept rows, combine skipping dropped pairs. Returns (y, S, g, inv)."""
+    h = np.asarray(h, dtype=np.float64)
+    z = router_logits(h, W_r, b_r)
+    S, g, _, _ = route(z, k, score_kind, norm, sel_bias)
+    counts, offsets, row_token, inv = dispatch_capacity(S, W_gate.shape[0], C)
+    y_rows = expert_rows(h[row_token], offsets, W_gate, W_up, W_down)
+    y = np.zeros_like(h)
+    if shared is not None:
+        y += swiglu_expert(h, *shared)
+    for t in range(h.shape[0]):
+        for j in range(k):
+            if inv[t, j] >= 0:
+                y[t] += g[t, j] * y_rows[inv[t, j]]
+    return y, S, g, inv

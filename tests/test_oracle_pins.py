@@ -510,3 +510,52 @@ def test_grouped_brute_force_and_errors():
         O.select_topk_grouped(np.zeros((1, 8)), 5, 4, 2)      # 2 groups x 2 = 4 < 5
     with pytest.raises(ValueError):
         O.select_topk_grouped(np.zeros((1, 9)), 2, 4, 2)      # 9 experts, 4 groups
+
+
+# ------------------------------------------------------------ capacity ---
+def test_capacity_formula():
+    assert O.expert_capacity(4, 2, 4, 1.0) == 2
+    assert O.expert_capacity(4, 2, 4, 1.25) == 3          # ceil(2.5)
+    assert O.expert_capacity(4096, 2, 8, 1.0) == 1024
+    assert O.expert_capacity(10, 1, 3, 1.0) == 4          # ceil(10/3)
+
+
+def test_page1_dispatch_table_with_capacity_two():
+    gd = load_golden("page1_dispatch_table.json")
+    S, _ = _choices(gd)
+    counts, offsets, row_token, inv = O.dispatch_capacity(S, gd["N"], 2)
+    # E2 receives T0, T1, T3 in token order; with C = 2 the pair of T3 is dropped
+    assert counts.tolist() == [2, 2, 2, 1]
+    assert row_token.tolist() == [0, 2, 1, 3, 0, 1, 2]
+    assert inv[3].tolist() == [-1, 3]                     # T3: (E2 dropped, E1 kept)
+    assert (inv >= 0).sum() == 7
+
+
+def test_capacity_large_is_dropless_and_zero_drops_all():
+    rng = np.random.default_rng(41)
+    S = np.array([rng.permutation(6)[:2] for _ in range(30)])
+    c0, o0, r0, i0 = O.dispatch(S, 6)
+    c1, o1, r1, i1 = O.dispatch_capacity(S, 6, 10 ** 6)
+    assert c0.tolist() == c1.tolist() and r0.tolist() == r1.tolist() and (i0 == i1).all()
+    c2, o2, r2, i2 = O.dispatch_capacity(S, 6, 0)
+    assert c2.sum() == 0 and (i2 == -1).all() and r2.size == 0
+
+
+def test_capacity_layer_brute_force_and_limits():
+    rng = np.random.default_rng(42)
+    h, W_r, Wg, Wu, Wd, sh = _tiny(rng, 14, 5, 4, 3, shared=True)
+    y_full, _, _, _ = O.moe_forward(h, W_r, Wg, Wu, Wd, 2, shared=sh)
+    y_big, _, _, inv_big = O.moe_forward_capacity(h, W_r, Wg, Wu, Wd, 2, 100, shared=sh)
+    np.testing.assert_allclose(y_big, y_full, atol=1e-12)
+    y0, _, _, _ = O.moe_forward_capacity(h, W_r, Wg, Wu, Wd, 2, 0, shared=sh)
+    np.testing.assert_allclose(y0, O.swiglu_expert(h, *sh), atol=1e-12)
+    # brute force for C = 3: per expert keep the 3 lowest-index tokens
+    C = 3
+    y3, S, g, inv = O.moe_forward_capacity(h, W_r, Wg, Wu, Wd, 2, C, shared=sh)
+    ref = O.swiglu_expert(h, *sh)
+    for e in range(4):
+        toks = [t for t in range(14) for j in range(2) if S[t, j] == e][:C]
+        for t in toks:
+            j = list(S[t]).index(e)
+            ref[t] += g[t, j] * O.swiglu_expert(h[t:t + 1], Wg[e], Wu[e], Wd[e])[0]
+    np.testing.assert_allclose(y3, ref, atol=1e-12)
