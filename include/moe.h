@@ -150,6 +150,18 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* h, const int3
                                 int32_t* counts, int32_t* offsets, int32_t* row_token,
                                 int32_t* inv, void* x_disp, cudaStream_t stream);
 
+/* Dispatch with an expert capacity ([P1] §六 Expert Capacity: C =
+ * ceil(capacity_factor * T * k / N); tokens beyond it may be dropped, the
+ * policy is left to the implementation). Each expert keeps its first
+ * `capacity` (token, slot) pairs in token order; the rest are dropped:
+ * inv[t*k + j] = -1 and no row is written for them. counts/offsets describe the
+ * kept rows only (sum counts = kept pairs). Otherwise as moe_dispatch.
+ * capacity in [0, 2^31]; 0 drops every pair. */
+moe_status moe_dispatch_capacity(const moe_config* cfg, int64_t capacity, const void* h,
+                                 const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                 int32_t* row_token, int32_t* inv, void* x_disp, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream);
+
 /* Stage 5+6: every expert's SwiGLU FFN over its dispatched rows, as one
  * grouped GEMM pair on the tensor cores (tcgen05, TMA-fed).
  * [P1] §一 E_i(h) = W_down (SiLU(W_gate h) * W_up h); [P1] §十二 Grouped GEMM;
@@ -234,6 +246,18 @@ moe_status moe_route_grouped(const moe_config* cfg, const moe_group_config* grp,
  *   Deterministic (fixed summation order). ws: per-block partial sums. */
 moe_status moe_route_stats(const moe_config* cfg, const float* logits, const int32_t* idx,
                            float* stats, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* moe_forward with an expert capacity: dropped (token, slot) pairs contribute
+ * nothing; gates are not renormalised over the kept experts; a token whose
+ * pairs are all dropped gets the shared expert's output only (zero without
+ * one), i.e. only its residual path in the surrounding block. counts = kept
+ * rows per expert. */
+moe_status moe_forward_capacity(const moe_config* cfg, int64_t capacity, const void* h,
+                                const void* W_r, const float* b_r, const float* sel_bias,
+                                const void* W_gate, const void* W_up, const void* W_down,
+                                const void* Ws_gate, const void* Ws_up, const void* Ws_down,
+                                void* out, float* logits_out, int32_t* idx, float* gate,
+                                int32_t* counts, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, copies the workspace's device status word into
  * *device_status (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK) and clears

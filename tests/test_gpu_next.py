@@ -151,3 +151,102 @@ def test_grouped_rejects_too_few_candidates(cuda_lib):
     grp = api.make_group_config(4, 2, "max")          # 2 groups x 2 experts = 4 < 5
     assert lib.moe_route_grouped(ctypes.byref(cfg), ctypes.byref(grp), None, None, None, None,
                                  fake, None, fake, fake, None, 0, None) == api.MOE_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------- capacity ---
+def _dispatch_cap(cfg, C, idx, h):
+    dev = "cuda"
+    R = cfg.T * cfg.k
+    ws = api.alloc_workspace(cfg, dev)
+    out = dict(counts=torch.empty(cfg.N, dtype=torch.int32, device=dev),
+               offsets=torch.empty(cfg.N + 1, dtype=torch.int32, device=dev),
+               row_token=torch.full((R,), -7, dtype=torch.int32, device=dev),
+               inv=torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev),
+               x_disp=torch.zeros((R, cfg.d), dtype=h.dtype, device=dev))
+    api.moe_dispatch_capacity(cfg, C, h.to(dev), idx.to(dev), out["counts"], out["offsets"],
+                              out["row_token"], out["inv"], out["x_disp"], ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    return out
+
+
+def test_capacity_page1_table(cuda_lib):
+    from conftest import load_golden
+    gd = load_golden("page1_dispatch_table.json")
+    idx = torch.tensor([[e for e, _ in row] for row in gd["choices"]], dtype=torch.int32)
+    h = torch.arange(32, dtype=torch.float32).reshape(4, 8).to(torch.bfloat16)
+    r = _dispatch_cap(api.make_config(4, 8, 4, 2, 8), 2, idx, h)
+    assert np_i(r["counts"]).tolist() == [2, 2, 2, 1]
+    kept = int(np_i(r["offsets"])[-1])
+    assert np_i(r["row_token"])[:kept].tolist() == [0, 2, 1, 3, 0, 1, 2]
+    assert np_i(r["inv"])[3].tolist() == [-1, 3]
+
+
+@pytest.mark.parametrize("T,N,k,C", [(3000, 8, 2, 0), (3000, 8, 2, 700), (3000, 8, 2, 10 ** 6),
+                                     (1000, 128, 8, 50), (513, 64, 1, 6)])
+def test_capacity_dispatch_random_exact(cuda_lib, T, N, k, C):
+    gen = torch.Generator().manual_seed(T + C)
+    # skewed routing so that some experts overflow
+    w = torch.arange(N, 0, -1, dtype=torch.float64) ** 2
+    idx = torch.stack([torch.multinomial(w, k, replacement=False, generator=gen)
+                       for _ in range(T)]).to(torch.int32)
+    h = torch.randn((T, 16), generator=gen).to(torch.bfloat16)
+    r = _dispatch_cap(api.make_config(T, 16, N, k, 8), C, idx, h)
+    counts, offsets, row_token, inv = O.dispatch_capacity(idx.numpy(), N, C)
+    assert np_i(r["counts"]).tolist() == counts.tolist()
+    assert np_i(r["offsets"]).tolist() == offsets.tolist()
+    kept = int(offsets[-1])
+    assert np_i(r["row_token"])[:kept].tolist() == row_token.tolist()
+    assert (np_i(r["inv"]) == inv).all()
+    assert torch.equal(r["x_disp"][:kept].cpu(), h[torch.from_numpy(row_token)])
+
+
+@pytest.mark.parametrize("cf", [0.5, 1.0, 1.25])
+def test_capacity_layer_vs_oracle(cuda_lib, cf):
+    w = Workload("cap", T=700, d=128, N=8, F=128, k=2, F_sh=128, score="sigmoid",
+                 bias_zipf_s=1.1, bias_beta=0.5)
+    cfg = api.config_for(w)
+    C = api.expert_capacity(w.T, w.k, w.N, cf)
+    inp = synth.make_inputs(w, seed=6, device="cpu")
+    gin = {k_: (v.cuda() if isinstance(v, torch.Tensor) else v) for k_, v in inp.items()}
+    ws = api.alloc_workspace(cfg, "cuda")
+    outs = api.alloc_outputs(cfg, "cuda", torch.bfloat16)
+    api.forward_capacity(cfg, C, gin, outs, ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    o = {k_: to_f64(v) for k_, v in inp.items()}
+    idx = np_i(outs["idx"])
+    z = O.router_logits(o["h"], o["W_r"])
+    g = O.gates_from_scores(O.scores(z, w.score), idx, w.norm)
+    counts, offsets, row_token, inv = O.dispatch_capacity(idx, w.N, C)
+    assert np_i(outs["counts"]).tolist() == counts.tolist()
+    y_rows = O.expert_rows(o["h"][row_token], offsets, o["W_gate"], o["W_up"], o["W_down"])
+    ysh = O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"])
+    ref = ysh.copy()
+    mag = np.abs(ysh)
+    for t in range(w.T):
+        for j in range(w.k):
+            if inv[t, j] >= 0:
+                ref[t] += g[t, j] * y_rows[inv[t, j]]
+                mag[t] += abs(g[t, j]) * np.abs(y_rows[inv[t, j]])
+    from gpu_helpers import BF16_TOL, assert_layer_close
+    assert_layer_close(np_f(outs["out"]), ref, mag, BF16_TOL, f"capacity cf={cf}")
+    dropped = int((inv < 0).sum())
+    print(f"cf={cf}: C={C}, dropped {dropped} of {w.T * w.k} pairs")
+    if cf < 1:
+        assert dropped > 0
+
+
+def test_capacity_unlimited_equals_dropless_forward(cuda_lib):
+    w = Workload("cap2", T=400, d=128, N=8, F=128, k=2)
+    cfg = api.config_for(w)
+    inp = {k_: (v.cuda() if isinstance(v, torch.Tensor) else v)
+           for k_, v in synth.make_inputs(w, seed=7).items()}
+    ws = api.alloc_workspace(cfg, "cuda")
+    a = api.alloc_outputs(cfg, "cuda", torch.bfloat16)
+    b = api.alloc_outputs(cfg, "cuda", torch.bfloat16)
+    api.forward(cfg, inp, a, ws)
+    api.forward_capacity(cfg, w.T * w.k, inp, b, ws)
+    torch.cuda.synchronize()
+    for key in ("out", "idx", "gate", "counts"):
+        assert torch.equal(a[key], b[key])

@@ -32,7 +32,8 @@ NORMS = {"selected": 0, "none": 1}
 ENTRY_POINTS = (
     "moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
     "moe_forward", "moe_read_status", "moe_selftest_wait_timeout", "moe_status_string",
-    "moe_dispatch_noalloc", "moe_route_stats", "moe_route_grouped",
+    "moe_dispatch_noalloc", "moe_route_stats", "moe_route_grouped", "moe_dispatch_capacity",
+    "moe_forward_capacity",
 )
 
 
@@ -81,6 +82,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_dispatch.argtypes = [cfgp] + [_vp] * 7 + [_vp, _sz, _vp]
     lib.moe_dispatch_noalloc.argtypes = [cfgp] + [_vp] * 7 + [_vp]
     lib.moe_route_stats.argtypes = [cfgp] + [_vp] * 3 + [_vp, _sz, _vp]
+    lib.moe_dispatch_capacity.argtypes = [cfgp, ctypes.c_int64] + [_vp] * 7 + [_vp, _sz, _vp]
+    lib.moe_forward_capacity.argtypes = [cfgp, ctypes.c_int64] + [_vp] * 15 + [_vp, _sz, _vp]
     lib.moe_route_grouped.argtypes = [cfgp, ctypes.POINTER(MoeGroupConfig)] + [_vp] * 8 + \
         [_vp, _sz, _vp]
     lib.moe_expert_ffn.argtypes = [cfgp] + [_vp] * 11 + [_vp, _sz, _vp]
@@ -197,6 +200,30 @@ def moe_route_grouped(cfg, grp, h, W_r, b_r, sel_bias, logits_in, logits_out, id
                                  _p(sel_bias), _p(logits_in), _p(logits_out), _p(idx), _p(gate),
                                  _p(ws), 0 if ws is None else ws.numel(), _stream(stream))
     _check(s, "moe_route_grouped")
+
+
+def expert_capacity(T: int, k: int, N: int, capacity_factor: float) -> int:
+    """C = ceil(capacity_factor * T * k / N)."""
+    import math
+    return int(math.ceil(capacity_factor * T * k / N))
+
+
+def moe_dispatch_capacity(cfg, capacity, h, idx, counts, offsets, row_token, inv, x_disp, ws,
+                          stream=None):
+    s = load().moe_dispatch_capacity(ctypes.byref(cfg), int(capacity), _p(h), _p(idx),
+                                     _p(counts), _p(offsets), _p(row_token), _p(inv), _p(x_disp),
+                                     _p(ws), ws.numel(), _stream(stream))
+    _check(s, "moe_dispatch_capacity")
+
+
+def forward_capacity(cfg, capacity, inp: dict, outs: "Outputs", ws, stream=None):
+    s = load().moe_forward_capacity(
+        ctypes.byref(cfg), int(capacity), _p(inp["h"]), _p(inp["W_r"]), _p(inp.get("b_r")),
+        _p(inp.get("sel_bias")), _p(inp["W_gate"]), _p(inp["W_up"]), _p(inp["W_down"]),
+        _p(inp.get("Ws_gate")), _p(inp.get("Ws_up")), _p(inp.get("Ws_down")), _p(outs["out"]),
+        _p(outs.get("logits")), _p(outs["idx"]), _p(outs["gate"]), _p(outs.get("counts")), _p(ws),
+        ws.numel(), _stream(stream))
+    _check(s, "moe_forward_capacity")
 
 
 def moe_route_stats(cfg, logits, idx, stats, ws, stream=None):

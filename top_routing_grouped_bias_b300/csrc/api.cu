@@ -65,7 +65,8 @@ moe_status route_impl(const moe_config* cfg, const void* h, const void* W_r, con
 
 moe_status dispatch_impl(const moe_config* cfg, const void* h, const int32_t* idx, int32_t* counts,
                          int32_t* offsets, int32_t* row_token, int32_t* inv, void* x_disp,
-                         void* ws, const WsLayout& L, cudaStream_t stream) {
+                         void* ws, const WsLayout& L, cudaStream_t stream,
+                         int64_t capacity = -1) {
   if (!ok_f32(idx) || !ok_f32(counts) || !ok_f32(offsets) || !ok_f32(row_token) || !ok_f32(inv))
     return MOE_ERR_INVALID_ARG;
   if (x_disp != nullptr && (!ok_tensor(x_disp) || !ok_tensor(h))) return MOE_ERR_INVALID_ARG;
@@ -74,6 +75,8 @@ moe_status dispatch_impl(const moe_config* cfg, const void* h, const int32_t* id
   a.inv = inv; a.x_disp = x_disp; a.block_base = at<int32_t>(ws, L.block_base);
   a.status = at<int32_t>(ws, L.status);
   a.T = cfg->T; a.d = cfg->d; a.N = cfg->N; a.k = cfg->k; a.dtype = cfg->dtype;
+  a.cap_enabled = capacity >= 0 ? 1 : 0;
+  a.capacity = capacity;
   return from_cuda(launch_dispatch(a, stream));
 }
 
@@ -165,12 +168,13 @@ moe_status moe_combine(const moe_config* cfg, const void* y_rows, const int32_t*
   return combine_impl(cfg, y_rows, inv, gate, y_shared, out, stream);
 }
 
-moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r, const float* b_r,
-                       const float* sel_bias, const void* W_gate, const void* W_up,
-                       const void* W_down, const void* Ws_gate, const void* Ws_up,
-                       const void* Ws_down, void* out, float* logits_out, int32_t* idx,
-                       float* gate, int32_t* counts, void* ws, size_t ws_bytes,
-                       cudaStream_t stream) {
+namespace {
+moe_status forward_impl(const moe_config* cfg, int64_t capacity, const void* h, const void* W_r,
+                        const float* b_r, const float* sel_bias, const void* W_gate,
+                        const void* W_up, const void* W_down, const void* Ws_gate,
+                        const void* Ws_up, const void* Ws_down, void* out, float* logits_out,
+                        int32_t* idx, float* gate, int32_t* counts, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
   moe_status s = check_config(cfg);
   if (s != MOE_OK) return s;
   if (!ok_tensor(h) || !ok_tensor(W_r) || !ok_tensor(W_gate) || !ok_tensor(W_up) ||
@@ -193,13 +197,14 @@ moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r, co
   s = route_impl(cfg, h, W_r, b_r, sel_bias, nullptr, logits_out, idx, gate,
                  at<int32_t>(ws, L.status), stream);
   if (s != MOE_OK) return s;
-  s = dispatch_impl(cfg, h, idx, cnt, offsets, row_token, inv, x_disp, ws, L, stream);
+  s = dispatch_impl(cfg, h, idx, cnt, offsets, row_token, inv, x_disp, ws, L, stream, capacity);
   if (s != MOE_OK) return s;
   s = ffn_impl(cfg, x_disp, offsets, W_gate, W_up, W_down, y_rows, h, Ws_gate, Ws_up, Ws_down,
                y_sh, ws, L, stream);
   if (s != MOE_OK) return s;
   return combine_impl(cfg, y_rows, inv, gate, y_sh, out, stream);
 }
+}  // namespace
 
 moe_status moe_route_grouped(const moe_config* cfg, const moe_group_config* grp, const void* h,
                              const void* W_r, const float* b_r, const float* sel_bias,
@@ -264,6 +269,40 @@ moe_status moe_route_stats(const moe_config* cfg, const float* logits, const int
   a.logits = logits; a.idx = idx; a.out = stats; a.partial = at<float>(ws, L.stats);
   a.T = cfg->T; a.N = cfg->N; a.k = cfg->k; a.score = cfg->score;
   return from_cuda(launch_route_stats(a, stream));
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r, const float* b_r,
+                       const float* sel_bias, const void* W_gate, const void* W_up,
+                       const void* W_down, const void* Ws_gate, const void* Ws_up,
+                       const void* Ws_down, void* out, float* logits_out, int32_t* idx,
+                       float* gate, int32_t* counts, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  return forward_impl(cfg, -1, h, W_r, b_r, sel_bias, W_gate, W_up, W_down, Ws_gate, Ws_up,
+                      Ws_down, out, logits_out, idx, gate, counts, ws, ws_bytes, stream);
+}
+
+moe_status moe_forward_capacity(const moe_config* cfg, int64_t capacity, const void* h,
+                                const void* W_r, const float* b_r, const float* sel_bias,
+                                const void* W_gate, const void* W_up, const void* W_down,
+                                const void* Ws_gate, const void* Ws_up, const void* Ws_down,
+                                void* out, float* logits_out, int32_t* idx, float* gate,
+                                int32_t* counts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (capacity < 0 || capacity > (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
+  return forward_impl(cfg, capacity, h, W_r, b_r, sel_bias, W_gate, W_up, W_down, Ws_gate, Ws_up,
+                      Ws_down, out, logits_out, idx, gate, counts, ws, ws_bytes, stream);
+}
+
+moe_status moe_dispatch_capacity(const moe_config* cfg, int64_t capacity, const void* h,
+                                 const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                 int32_t* row_token, int32_t* inv, void* x_disp, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (capacity < 0 || capacity > (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  if (!ws_ok(ws, ws_bytes, L.end_dispatch)) return MOE_ERR_WORKSPACE;
+  return dispatch_impl(cfg, h, idx, counts, offsets, row_token, inv, x_disp, ws, L, stream,
+                       capacity);
 }
 
 moe_status moe_read_status(void* ws, size_t ws_bytes, int32_t* device_status, cudaStream_t stream) {

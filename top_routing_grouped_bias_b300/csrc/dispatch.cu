@@ -5,11 +5,12 @@
 //
 // Deterministic counting sort in three launches, no atomics on the ordering:
 //   1. count    per block of 256 tokens, per-expert pair counts -> base[b][e]
-//   2. scan     counts[e] = sum_b, offsets = exclusive scan over e, and
-//               base[b][e] = offsets[e] + sum_{b' < b} count[b'][e]
+//   2. scan     counts[e] = sum_b (capped at the capacity when one is set),
+//               offsets = exclusive scan over e, base[b][e] = sum_{b' < b} count[b'][e]
 //   3. permute  per block: per-warp counts, scan over warps, then the rank of
 //               each pair among earlier pairs of the same expert in its warp;
-//               row = base + warp prefix + rank. Writes row_token and inv.
+//               rank = base + warp prefix + in-warp rank; row = offsets[e] + rank,
+//               or inv = -1 when rank >= capacity. Writes row_token and inv.
 //   4. gather   one thread per 16-byte vector of h: reads h[t] once, writes
 //               it to the token's k dispatched rows.
 // The row of (t, e) is offsets[e] + #{t' < t : e in S_t'}, i.e. rows are
@@ -57,7 +58,8 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(DispatchArgs a, int
       *p = run;
       run += c;
     }
-    tot[e] = run;
+    // rows kept for this expert: all of them, or its first `capacity` pairs
+    tot[e] = a.cap_enabled && run > a.capacity ? static_cast<int>(a.capacity) : run;
   }
   __syncthreads();
   // exclusive scan of tot[0..N) with one block: each thread owns a contiguous chunk
@@ -93,12 +95,6 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(DispatchArgs a, int
     run += tot[e];
   }
   if (hi == N && lo < hi) a.offsets[N] = run;  // the owner of expert N-1 (N >= 1)
-  __syncthreads();
-  // add the expert offsets to every block's base
-  for (int b = 0; b < nb; ++b) {
-    int32_t* p = a.block_base + static_cast<size_t>(b) * N;
-    for (int e = threadIdx.x; e < N; e += blockDim.x) p[e] += a.offsets[e];
-  }
 }
 
 __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
@@ -119,7 +115,8 @@ __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
     if (e >= 0) atomicAdd(&whist[warp * N + e], 1);
   }
   __syncthreads();
-  // per expert: exclusive scan over warps, plus the block base
+  // per expert: exclusive scan over warps, plus the block's rank base (the
+  // number of the expert's pairs in earlier blocks)
   const int32_t* base = a.block_base + static_cast<size_t>(blockIdx.x) * N;
   for (int e = threadIdx.x; e < N; e += blockDim.x) {
     int run = base[e];
@@ -141,7 +138,12 @@ __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
       int rank = 0;
       for (int l = 0; l < lane; ++l)
         for (int jj = 0; jj < k; ++jj) rank += (wid[l * k + jj] == e);
-      const int row = whist[warp * N + e] + rank;
+      rank += whist[warp * N + e];  // position among all of expert e's pairs
+      if (a.cap_enabled && rank >= a.capacity) {
+        a.inv[t * k + j] = -1;  // beyond the expert's capacity: dropped
+        continue;
+      }
+      const int row = a.offsets[e] + rank;
       a.row_token[row] = static_cast<int32_t>(t);
       a.inv[t * k + j] = row;
     }

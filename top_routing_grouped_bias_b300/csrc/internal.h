@@ -90,6 +90,8 @@ struct DispatchArgs {
   int32_t* status;      // device status word (index checks)
   int64_t T;
   int32_t d, N, k, dtype;
+  int32_t cap_enabled;  // 0 (value-initialised default): dropless
+  int64_t capacity;     // rows kept per expert when cap_enabled
 };
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
 
