@@ -482,3 +482,41 @@ def moe_forward_capacity(h, W_r, W_gate, W_up, W_down, k, C, score_kind=SOFTMAX,
             if inv[t, j] >= 0:
                 y[t] += g[t, j] * y_rows[inv[t, j]]
     return y, S, g, inv
+
+
+# --------------------------------------------------------------------------
+# Expert Choice routing
+# --------------------------------------------------------------------------
+def expert_choice(z, C, score_kind=SOFTMAX):
+    """Expert Choice ([P1] §九 routing table; [P2] "Token 选 expert，还是 expert
+    选 token"): each expert picks the C tokens with the highest router score
+    for it; a token can be picked by any number of experts (0..N).
+    Scores p = softmax over experts per token (or sigmoid). Reading taken:
+    equal scores go to the lower token index; an expert's picked tokens are
+    listed in ascending token order (the order does not change the output).
+    Returns (tokens [N, C] int64, gates [N, C] = p[token, expert], p)."""
+    p = scores(z, score_kind)
+    T, N = p.shape
+    if not 0 <= C <= T:
+        raise ValueError("need 0 <= C <= T")
+    picked = select_topk(p.T, C) if C > 0 else np.zeros((N, 0), dtype=np.int64)
+    tokens = np.sort(picked, axis=1)
+    gates = np.take_along_axis(p.T, tokens, axis=1)
+    return tokens, gates, p
+
+
+def moe_forward_expert_choice(h, W_r, W_gate, W_up, W_down, C, score_kind=SOFTMAX,
+                              b_r=None, shared=None):
+    """y_t = [sum_s E_s(h_t)] + sum_{e : t picked by e} p_{t,e} E_e(h_t)."""
+    h = np.asarray(h, dtype=np.float64)
+    z = router_logits(h, W_r, b_r)
+    tokens, gates, _ = expert_choice(z, C, score_kind)
+    y = np.zeros_like(h)
+    if shared is not None:
+        y += swiglu_expert(h, *shared)
+    for e in range(W_gate.shape[0]):
+        toks = tokens[e]
+        if toks.size:
+            np.add.at(y, toks, gates[e][:, None] * swiglu_expert(h[toks], W_gate[e], W_up[e],
+                                                                  W_down[e]))
+    return y, tokens, gates

@@ -559,3 +559,43 @@ def test_capacity_layer_brute_force_and_limits():
             j = list(S[t]).index(e)
             ref[t] += g[t, j] * O.swiglu_expert(h[t:t + 1], Wg[e], Wu[e], Wd[e])[0]
     np.testing.assert_allclose(y3, ref, atol=1e-12)
+
+
+# ---------------------------------------------------------- expert choice ---
+def test_expert_choice_hand_example():
+    # 3 tokens, 2 experts, each expert picks 2 tokens by its column of p
+    z = np.log(np.array([[0.7, 0.3], [0.2, 0.8], [0.6, 0.4]]))
+    tokens, gates, p = O.expert_choice(z, 2)
+    assert tokens.tolist() == [[0, 2], [1, 2]]          # E0: 0.7, 0.6; E1: 0.8, 0.4
+    np.testing.assert_allclose(gates, [[0.7, 0.6], [0.8, 0.4]], atol=1e-15)
+    # token 2 is picked by both experts; no token is left out here, none picked thrice
+
+
+def test_expert_choice_ties_lower_token_and_loads_fixed():
+    z = np.zeros((6, 3))                                 # every score equal
+    tokens, _, _ = O.expert_choice(z, 4)
+    assert tokens.tolist() == [[0, 1, 2, 3]] * 3
+    rng = np.random.default_rng(51)
+    z = rng.standard_normal((40, 5))
+    tokens, gates, p = O.expert_choice(z, 7)
+    assert tokens.shape == (5, 7)                        # every expert exactly C tokens
+    for e in range(5):
+        # brute force: the 7 largest p[:, e] with lower index first on ties
+        assert set(tokens[e].tolist()) == set(O.topk_by_rank_count(p[:, e], 7))
+
+
+def test_expert_choice_layer_vs_dense_mask():
+    rng = np.random.default_rng(52)
+    h, W_r, Wg, Wu, Wd, sh = _tiny(rng, 12, 5, 4, 3, shared=True)
+    y, tokens, gates = O.moe_forward_expert_choice(h, W_r, Wg, Wu, Wd, 5, shared=sh)
+    z = O.router_logits(h, W_r)
+    p = O.softmax(z)
+    G = np.zeros((12, 4))
+    for e in range(4):
+        G[tokens[e], e] = p[tokens[e], e]
+    ref = O.swiglu_expert(h, *sh)
+    for e in range(4):
+        ref += G[:, e:e + 1] * O.swiglu_expert(h, Wg[e], Wu[e], Wd[e])
+    np.testing.assert_allclose(y, ref, atol=1e-12)
+    y0, _, _ = O.moe_forward_expert_choice(h, W_r, Wg, Wu, Wd, 0, shared=sh)
+    np.testing.assert_allclose(y0, O.swiglu_expert(h, *sh), atol=1e-12)
