@@ -259,6 +259,23 @@ moe_status moe_forward_capacity(const moe_config* cfg, int64_t capacity, const v
                                 void* out, float* logits_out, int32_t* idx, float* gate,
                                 int32_t* counts, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* The layer with Expert Choice routing ([P1] §九 routing table; [P2] last
+ * section): scores p = softmax (or sigmoid, cfg->score) of the logits; every
+ * expert picks the `capacity` tokens with the highest p for it (equal scores:
+ * lower token index); y_t = [shared] + sum over experts e that picked t of
+ * p_{t,e} E_e(h_t). A token may be picked by no expert (output: shared expert
+ * or zero) or by several. cfg->k is the average experts per token the
+ * workspace is sized for: require capacity * N <= T * k and capacity <= T.
+ *   tokens_out [N, capacity] int32 or NULL: each expert's picked tokens in
+ *              ascending order; gates_out [N, capacity] fp32 or NULL: their p
+ *   sel_bias and cfg->norm do not apply. ws: moe_workspace_size(cfg) bytes. */
+moe_status moe_forward_expert_choice(const moe_config* cfg, int64_t capacity, const void* h,
+                                     const void* W_r, const float* b_r, const void* W_gate,
+                                     const void* W_up, const void* W_down, const void* Ws_gate,
+                                     const void* Ws_up, const void* Ws_down, void* out,
+                                     float* logits_out, int32_t* tokens_out, float* gates_out,
+                                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, copies the workspace's device status word into
  * *device_status (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK) and clears
  * it. Returns MOE_ERR_CUDA if the synchronisation or copy fails. */

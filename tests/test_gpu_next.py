@@ -250,3 +250,96 @@ def test_capacity_unlimited_equals_dropless_forward(cuda_lib):
     torch.cuda.synchronize()
     for key in ("out", "idx", "gate", "counts"):
         assert torch.equal(a[key], b[key])
+
+
+# --------------------------------------------------------- expert choice ---
+def _ec_run(cfg, C, inp):
+    dev = "cuda"
+    ws = api.alloc_workspace(cfg, dev)
+    tdt = torch.float32 if cfg.dtype == api.DTYPES["f32"] else torch.bfloat16
+    out = torch.empty((cfg.T, cfg.d), dtype=tdt, device=dev)
+    logits = torch.empty((cfg.T, cfg.N), dtype=torch.float32, device=dev)
+    tokens = torch.full((cfg.N, max(C, 1)), -1, dtype=torch.int32, device=dev)
+    gates = torch.zeros((cfg.N, max(C, 1)), dtype=torch.float32, device=dev)
+    gin = {k_: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k_, v in inp.items()}
+    api.forward_expert_choice(cfg, C, gin, out, ws, logits, tokens, gates)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    return out, logits, tokens[:, :C], gates[:, :C]
+
+
+def _ec_check_selection(z64, score, C, tokens, gates):
+    """Each expert's picked set equals the oracle's, except where the oracle's
+    C-th and (C+1)-th scores are within what fp32 scoring can move."""
+    p = O.scores(z64, score)
+    ref_tokens, _, _ = O.expert_choice(z64, C, score)
+    amb = 0
+    for e in range(p.shape[1]):
+        got = np_i(tokens)[e]
+        assert (np.diff(got) > 0).all(), "picked tokens must be ascending and distinct"
+        col = -np.sort(-p[:, e])
+        gap = col[C - 1] - col[C] if C < p.shape[0] else np.inf
+        if gap > 4e-6:
+            assert set(got.tolist()) == set(ref_tokens[e].tolist()), f"expert {e}"
+        else:
+            amb += 1
+            assert (p[got, e] >= col[C - 1] - 4e-6).all()
+        np.testing.assert_allclose(np_f(gates)[e], p[got, e], atol=1e-6, rtol=0)
+    return amb
+
+
+@pytest.mark.parametrize("score,shared", [("softmax", False), ("sigmoid", True)])
+def test_expert_choice_layer_vs_oracle(cuda_lib, score, shared):
+    w = Workload("ec", T=700, d=128, N=8, F=128, k=2, F_sh=128 if shared else 0, score=score)
+    cfg = api.config_for(w)
+    C = w.T * w.k // w.N
+    inp = synth.make_inputs(w, seed=8, device="cpu")
+    out, logits, tokens, gates = _ec_run(cfg, C, inp)
+    z = np_f(logits)
+    o = {k_: to_f64(v) for k_, v in inp.items()}
+    amb = _ec_check_selection(z, score, C, tokens, gates)
+    assert amb <= 1
+    # layer output with the GPU's (validated) picks, oracle fp64 scores and experts
+    p = O.scores(O.router_logits(o["h"], o["W_r"]), score)
+    ref = np.zeros((w.T, w.d)) if not shared else O.swiglu_expert(o["h"], o["Ws_gate"],
+                                                                  o["Ws_up"], o["Ws_down"])
+    mag = np.abs(ref)
+    tk = np_i(tokens)
+    for e in range(w.N):
+        ye = O.swiglu_expert(o["h"][tk[e]], o["W_gate"][e], o["W_up"][e], o["W_down"][e])
+        ref[tk[e]] += p[tk[e], e][:, None] * ye
+        mag[tk[e]] += p[tk[e], e][:, None] * np.abs(ye)
+    from gpu_helpers import BF16_TOL, assert_layer_close
+    assert_layer_close(np_f(out), ref, mag, BF16_TOL, "expert choice")
+
+
+def test_expert_choice_ties_and_empty(cuda_lib):
+    """Duplicated hidden rows give bitwise-equal scores: the lower token index
+    is picked first. C = 0 leaves only the shared expert."""
+    w = Workload("ec_ties", T=64, d=64, N=4, F=64, k=1, F_sh=64)
+    cfg = api.config_for(w)
+    inp = synth.make_inputs(w, seed=9, device="cpu")
+    inp["h"][1::2] = inp["h"][0::2]                 # tokens 2i and 2i+1 identical
+    C = 16
+    out, logits, tokens, gates = _ec_run(cfg, C, inp)
+    z = np_f(logits)
+    ref_tokens, _, _ = O.expert_choice(z, C, w.score)
+    assert (np_i(tokens) == ref_tokens).all()
+    out0, _, _, _ = _ec_run(cfg, 0, inp)
+    o = {k_: to_f64(v) for k_, v in inp.items()}
+    from gpu_helpers import BF16_TOL, assert_close_tol
+    assert_close_tol(np_f(out0), O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"]),
+                     BF16_TOL, "C = 0")
+
+
+def test_expert_choice_switch_sized(cuda_lib):
+    """Switch-sized batch (T = 65536, N = 128, d = 2048): every expert takes
+    exactly T/N tokens; picks and gates checked on every expert."""
+    w = synth.WORKLOADS["switch_top1"]
+    cfg = api.config_for(w)
+    C = w.T * w.k // w.N
+    inp = synth.make_inputs(w, seed=0, device="cuda")
+    out, logits, tokens, gates = _ec_run(cfg, C, inp)
+    amb = _ec_check_selection(np_f(logits), w.score, C, tokens, gates)
+    print(f"expert choice switch-sized: {amb} experts with a boundary within fp32 reach")
+    assert torch.isfinite(out.float()).all()

@@ -33,7 +33,7 @@ ENTRY_POINTS = (
     "moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
     "moe_forward", "moe_read_status", "moe_selftest_wait_timeout", "moe_status_string",
     "moe_dispatch_noalloc", "moe_route_stats", "moe_route_grouped", "moe_dispatch_capacity",
-    "moe_forward_capacity",
+    "moe_forward_capacity", "moe_forward_expert_choice",
 )
 
 
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_route_stats.argtypes = [cfgp] + [_vp] * 3 + [_vp, _sz, _vp]
     lib.moe_dispatch_capacity.argtypes = [cfgp, ctypes.c_int64] + [_vp] * 7 + [_vp, _sz, _vp]
     lib.moe_forward_capacity.argtypes = [cfgp, ctypes.c_int64] + [_vp] * 15 + [_vp, _sz, _vp]
+    lib.moe_forward_expert_choice.argtypes = [cfgp, ctypes.c_int64] + [_vp] * 13 + [_vp, _sz, _vp]
     lib.moe_route_grouped.argtypes = [cfgp, ctypes.POINTER(MoeGroupConfig)] + [_vp] * 8 + \
         [_vp, _sz, _vp]
     lib.moe_expert_ffn.argtypes = [cfgp] + [_vp] * 11 + [_vp, _sz, _vp]
@@ -224,6 +225,16 @@ def forward_capacity(cfg, capacity, inp: dict, outs: "Outputs", ws, stream=None)
         _p(outs.get("logits")), _p(outs["idx"]), _p(outs["gate"]), _p(outs.get("counts")), _p(ws),
         ws.numel(), _stream(stream))
     _check(s, "moe_forward_capacity")
+
+
+def forward_expert_choice(cfg, capacity, inp: dict, out, ws, logits=None, tokens=None,
+                          gates=None, stream=None):
+    s = load().moe_forward_expert_choice(
+        ctypes.byref(cfg), int(capacity), _p(inp["h"]), _p(inp["W_r"]), _p(inp.get("b_r")),
+        _p(inp["W_gate"]), _p(inp["W_up"]), _p(inp["W_down"]), _p(inp.get("Ws_gate")),
+        _p(inp.get("Ws_up")), _p(inp.get("Ws_down")), _p(out), _p(logits), _p(tokens), _p(gates),
+        _p(ws), ws.numel(), _stream(stream))
+    _check(s, "moe_forward_expert_choice")
 
 
 def moe_route_stats(cfg, logits, idx, stats, ws, stream=None):

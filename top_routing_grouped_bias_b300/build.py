@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libmoe_b300.so")
 SOURCES = ["api.cu", "route.cu", "dispatch.cu", "combine.cu", "grouped_gemm.cu",
-           "dispatch_noalloc.cu", "stats.cu"]
+           "dispatch_noalloc.cu", "stats.cu", "expert_choice.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -305,6 +305,64 @@ moe_status moe_dispatch_capacity(const moe_config* cfg, int64_t capacity, const 
                        capacity);
 }
 
+moe_status moe_forward_expert_choice(const moe_config* cfg, int64_t capacity, const void* h,
+                                     const void* W_r, const float* b_r, const void* W_gate,
+                                     const void* W_up, const void* W_down, const void* Ws_gate,
+                                     const void* Ws_up, const void* Ws_down, void* out,
+                                     float* logits_out, int32_t* tokens_out, float* gates_out,
+                                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (capacity < 0 || capacity > cfg->T || capacity * cfg->N > cfg->T * cfg->k)
+    return MOE_ERR_INVALID_ARG;
+  if (!ok_tensor(h) || !ok_tensor(W_r) || !ok_tensor(W_gate) || !ok_tensor(W_up) ||
+      !ok_tensor(W_down) || !ok_tensor(out) || !ok_opt_f32(logits_out) ||
+      !ok_opt_f32(tokens_out) || !ok_opt_f32(gates_out) || !ok_opt_f32(b_r))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->ffn_shared > 0 && (!ok_tensor(Ws_gate) || !ok_tensor(Ws_up) || !ok_tensor(Ws_down)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  if (!ws_ok(ws, ws_bytes, L.total)) return MOE_ERR_WORKSPACE;
+  if (cfg->T == 0) return MOE_OK;
+  float* z = logits_out != nullptr ? logits_out : at<float>(ws, L.logits);
+  // logits through the router (its top-k output goes to scratch)
+  s = route_impl(cfg, h, W_r, b_r, nullptr, nullptr, z, at<int32_t>(ws, L.row_token),
+                 at<float>(ws, L.inv), at<int32_t>(ws, L.status), stream);
+  if (s != MOE_OK) return s;
+  EcArgs e{};
+  e.logits = z;
+  e.scores_t = at<float>(ws, L.ec_scores);
+  e.choice = at<int32_t>(ws, L.ec_choice);
+  e.row_token = at<int32_t>(ws, L.row_token);
+  e.row_gate = at<float>(ws, L.inv);
+  e.offsets = at<int32_t>(ws, L.offsets);
+  e.tokens_out = tokens_out;
+  e.gates_out = gates_out;
+  e.h = h;
+  e.x_disp = at<void>(ws, L.x_disp);
+  e.y_rows = at<void>(ws, L.y_rows);
+  e.y_shared = cfg->ffn_shared > 0 ? at<void>(ws, L.y_sh) : nullptr;
+  e.out = out;
+  e.T = cfg->T; e.d = cfg->d; e.N = cfg->N; e.C = static_cast<int32_t>(capacity);
+  e.score = cfg->score; e.dtype = cfg->dtype;
+  s = from_cuda(launch_ec_select(e, stream));
+  if (s != MOE_OK) return s;
+  if (capacity > 0 || cfg->ffn_shared > 0) {
+    FfnArgs a{};
+    a.x_disp = e.x_disp; a.offsets = e.offsets; a.W_gate = W_gate; a.W_up = W_up;
+    a.W_down = W_down; a.y_rows = at<void>(ws, L.y_rows); a.h = h; a.Ws_gate = Ws_gate;
+    a.Ws_up = Ws_up; a.Ws_down = Ws_down; a.y_shared = const_cast<void*>(e.y_shared);
+    a.act = at<void>(ws, L.act); a.act_sh = at<void>(ws, L.act_sh);
+    a.status = at<int32_t>(ws, L.status);
+    a.T = cfg->T; a.d = cfg->d; a.N = cfg->N; a.k = cfg->k; a.F = cfg->ffn;
+    a.F_sh = cfg->ffn_shared; a.dtype = cfg->dtype;
+    a.rows = capacity * cfg->N > 0 ? capacity * cfg->N : 1;
+    s = from_cuda(launch_expert_ffn(a, stream));
+    if (s != MOE_OK) return s;
+  }
+  return from_cuda(launch_ec_combine(e, stream));
+}
+
 moe_status moe_read_status(void* ws, size_t ws_bytes, int32_t* device_status, cudaStream_t stream) {
   if (ws == nullptr || ws_bytes < 256 || device_status == nullptr) return MOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;

@@ -978,7 +978,7 @@ int num_sms() {
 
 cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
-  const int64_t R = a.T * a.k;
+  const int64_t R = a.rows > 0 ? a.rows : a.T * a.k;
   const bool sh = a.F_sh > 0;
   const int sms = num_sms();
   CUtensorMap m[6];

@@ -22,7 +22,7 @@ inline int elem_size(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 // expert FFN [status .. act_sh], forward everything.
 struct WsLayout {
   size_t status, block_base, stats, act, act_sh, offsets, counts, row_token, inv, x_disp, y_rows,
-      y_sh, logits;
+      y_sh, logits, ec_scores, ec_choice;
   size_t end_dispatch, end_ffn, total;
 };
 
@@ -52,6 +52,8 @@ inline WsLayout ws_layout(const moe_config& c) {
   L.y_rows = take(R * static_cast<size_t>(c.d) * e);
   L.y_sh = take(c.ffn_shared > 0 ? T * static_cast<size_t>(c.d) * e : 0);
   L.logits = take(T * static_cast<size_t>(c.N) * 4);
+  L.ec_scores = take(T * static_cast<size_t>(c.N) * 4);
+  L.ec_choice = take(T * static_cast<size_t>(c.N) * 4);
   L.total = o;
   return L;
 }
@@ -113,6 +115,7 @@ struct FfnArgs {
   int32_t* status;
   int64_t T;
   int32_t d, N, k, F, F_sh, dtype;
+  int64_t rows;  // dispatched rows when not T*k (0 = T*k)
 };
 cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream);
 
@@ -138,6 +141,27 @@ struct StatsArgs {
   int32_t N, k, score;
 };
 cudaError_t launch_route_stats(const StatsArgs& a, cudaStream_t stream);
+
+// ---- expert-choice routing ----
+struct EcArgs {
+  const float* logits;  // [T, N]
+  float* scores_t;      // [N, T] scratch
+  int32_t* choice;      // [T, N] scratch: row + 1 of (token, expert), 0 = not picked
+  int32_t* row_token;   // [N * C]
+  float* row_gate;      // [N * C]
+  int32_t* offsets;     // [N + 1]
+  int32_t* tokens_out;  // [N, C] or null
+  float* gates_out;     // [N, C] or null
+  const void* h;
+  void* x_disp;         // [N * C, d]
+  const void* y_rows;   // [N * C, d]
+  const void* y_shared; // [T, d] or null
+  void* out;            // [T, d]
+  int64_t T;
+  int32_t d, N, C, score, dtype;
+};
+cudaError_t launch_ec_select(const EcArgs& a, cudaStream_t stream);
+cudaError_t launch_ec_combine(const EcArgs& a, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t budget_ns, cudaStream_t stream);
 
