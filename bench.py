@@ -311,30 +311,33 @@ def bench_ours(args, w):
     assert api.read_status(ws) == api.MOE_OK
 
     # ---- end to end through the C ABI with host buffers ----
-    h_host = inp["h"].cpu().pin_memory()
-    out_host = torch.empty((w.T, w.d), dtype=tdt).pin_memory()
-    h_dev = torch.empty_like(inp["h"])
-    inp_e2e = dict(inp)
-    inp_e2e["h"] = h_dev
-
-    def e2e_step():
-        h_dev.copy_(h_host, non_blocking=True)
-        api.forward(cfg, inp_e2e, outs, ws, stream)
-        out_host.copy_(outs["out"], non_blocking=True)
-
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    # Every step copies its hidden states from pinned host memory and its
+    # output back; the copies of neighbouring steps overlap the compute.
+    h_hosts = [inp["h"].cpu().pin_memory() for _ in range(2)]
+    out_hosts = [torch.empty((w.T, w.d), dtype=tdt).pin_memory() for _ in range(2)]
+    weights = {k_: v for k_, v in inp.items() if k_ != "h"}
+    pipe = api.HostPipeline(cfg, weights, tdt, dev)
+    for i in range(max(1, args.warmup)):
+        pipe.step(i, h_hosts[i % 2], out_hosts[i % 2])
+    pipe.drain()
     torch.cuda.synchronize(dev)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(pipe.compute)
+    pipe.copy_in.wait_event(e0)   # the first copy of the timed region starts after e0
+    for i in range(args.steps):
+        pipe.step(i, h_hosts[i % 2], out_hosts[i % 2])
+    pipe.drain()
+    e1.record(pipe.compute)
     torch.cuda.synchronize(dev)
     barrier()
+    assert api.read_status(pipe.ws) == api.MOE_OK
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     e2e_value = aggregate_rate(w.T * args.steps, world, e2e_ms * args.steps / 1e3)
+    h_host = h_hosts[0]
+    out_host = out_hosts[0]
+
+    next_rows = time_next_rows(w, cfg, inp, ws, stream, dev, stage_ms)
 
     if rank != 0:
         return None
@@ -375,6 +378,7 @@ def bench_ours(args, w):
         "roofline": roof,
         "stages_ms": {"route": round(route_ms, 4), "dispatch": round(disp_ms, 4),
                       "grouped_gemm": round(ffn_ms, 4), "combine": round(comb_ms, 4)},
+        "next_rows": next_rows,
         "gpu_launches": KERNELS_PER_FORWARD * args.steps,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_host.numel() * h_host.element_size()),
@@ -382,6 +386,45 @@ def bench_ours(args, w):
         "clocks": clk.summary(),
     }
     return line
+
+
+def time_next_rows(w, cfg, inp, ws, stream, dev, stage_ms, reps=10):
+    """Device time of the rows beyond the core layer on the same batch:
+    routing statistics, group-limited routing, the layer with an expert
+    capacity (factor 1.25) and the layer with expert-choice routing."""
+    peaks, _ = load_peaks()
+    T, N, k = w.T, w.N, w.k
+    out = {}
+    logits = torch.empty((T, N), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, k), dtype=torch.float32, device=dev)
+    api.moe_route(cfg, inp["h"], inp["W_r"], None, inp["sel_bias"], None, logits, idx, gate, ws,
+                  stream)
+    stats = torch.empty(3 + 2 * N, dtype=torch.float32, device=dev)
+    ms = stage_ms(lambda: api.moe_route_stats(cfg, logits, idx, stats, ws, stream), reps)
+    by = T * N * 4 + T * k * 4
+    out["route_stats"] = {"ms": round(ms, 4), "GB/s": round(by / ms / 1e6, 1),
+                          "hbm_frac": round(by / ms / 1e6 / peaks["hbm_gbs"], 3)}
+    ng = next((g for g in (8, 4, 2) if N % g == 0 and (N // g) * (g // 2) >= k), 0)
+    if ng:
+        grp = api.make_group_config(ng, ng // 2, "topm_sum", min(2, N // ng))
+        ms = stage_ms(lambda: api.moe_route_grouped(cfg, grp, inp["h"], inp["W_r"], None,
+                                                    inp["sel_bias"], None, logits, idx, gate, ws,
+                                                    stream), reps)
+        out["route_grouped"] = {"ms": round(ms, 4), "groups": f"{ng} keep {ng // 2} top-2 sum"}
+    tdt = w.torch_dtype
+    outs = api.alloc_outputs(cfg, dev, tdt, logits=False)
+    C = api.expert_capacity(T, k, N, 1.25)
+    ms = stage_ms(lambda: api.forward_capacity(cfg, C, inp, outs, ws, stream), reps)
+    out["forward_capacity_1.25"] = {"ms": round(ms, 4), "tokens/s": round(T / ms * 1e3, 1),
+                                    "capacity": C}
+    C = T * k // N
+    y = torch.empty((T, w.d), dtype=tdt, device=dev)
+    ms = stage_ms(lambda: api.forward_expert_choice(cfg, C, inp, y, ws, stream=stream), reps)
+    out["forward_expert_choice"] = {"ms": round(ms, 4), "tokens/s": round(T / ms * 1e3, 1),
+                                    "capacity": C}
+    assert api.read_status(ws) == api.MOE_OK
+    return out
 
 
 def bench_reference(args, w):

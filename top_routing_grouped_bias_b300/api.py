@@ -280,3 +280,54 @@ def forward(cfg: MoeConfig, inp: dict, outs: Outputs, ws: torch.Tensor, stream=N
                 inp["W_up"], inp["W_down"], inp.get("Ws_gate"), inp.get("Ws_up"),
                 inp.get("Ws_down"), outs["out"], outs.get("logits"), outs["idx"], outs["gate"],
                 outs.get("counts"), ws, stream)
+
+
+class HostPipeline:
+    """moe_forward over batches that live in (pinned) host memory, with the
+    host-to-device copy of the next batch and the device-to-host copy of the
+    previous output running on their own streams while the current batch
+    computes. Two device buffers alternate; events order every reuse.
+
+    Only copies and launches are scheduled here; all arithmetic is the
+    library's moe_forward.
+    """
+
+    def __init__(self, cfg: MoeConfig, weights: dict, dtype=torch.bfloat16, device="cuda"):
+        dev = torch.device(device)
+        self.cfg, self.weights, self.dev = cfg, weights, dev
+        T, d = cfg.T, cfg.d
+        self.h_dev = [torch.empty((T, d), dtype=dtype, device=dev) for _ in range(2)]
+        self.outs = [alloc_outputs(cfg, dev, dtype, logits=False) for _ in range(2)]
+        self.ws = alloc_workspace(cfg, dev)
+        self.compute = torch.cuda.current_stream(dev)
+        self.copy_in = torch.cuda.Stream(dev)
+        self.copy_out = torch.cuda.Stream(dev)
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.in_ready, self.done, self.out_copied = ev(), ev(), ev()
+        self.used = [False, False]
+
+    def step(self, i: int, h_host: torch.Tensor, out_host: torch.Tensor):
+        b = i % 2
+        if self.used[b]:
+            self.copy_in.wait_event(self.done[b])            # h_dev[b] no longer read
+        with torch.cuda.stream(self.copy_in):
+            self.h_dev[b].copy_(h_host, non_blocking=True)
+            self.in_ready[b].record(self.copy_in)
+        self.compute.wait_event(self.in_ready[b])
+        if self.used[b]:
+            self.compute.wait_event(self.out_copied[b])      # outs[b] drained to the host
+        inp = dict(self.weights)
+        inp["h"] = self.h_dev[b]
+        forward(self.cfg, inp, self.outs[b], self.ws, self.compute)
+        self.done[b].record(self.compute)
+        self.copy_out.wait_event(self.done[b])
+        with torch.cuda.stream(self.copy_out):
+            out_host.copy_(self.outs[b]["out"], non_blocking=True)
+            self.out_copied[b].record(self.copy_out)
+        self.used[b] = True
+
+    def drain(self):
+        """Make the compute stream wait for every copy issued so far."""
+        for b in range(2):
+            if self.used[b]:
+                self.compute.wait_event(self.out_copied[b])
