@@ -329,3 +329,23 @@ def test_route_tensor_core_exact_ties(cuda_lib, score, N, k):
     np.testing.assert_allclose(np_f(gate), g, atol=1e-6, rtol=0)
     bound = logit_bound(to_f64(h), to_f64(W))
     assert (np.abs(z - O.router_logits(to_f64(h), to_f64(W))) <= bound).all()
+
+
+@pytest.mark.parametrize("name", ["switch_top1", "one_expert", "pair_ragged"])
+def test_fused_top1_forward_vs_oracle(cuda_lib, name):
+    """Top-1 without a shared expert: moe_forward writes g * E(h) from the down
+    pass directly. Checked against the oracle and against the staged path
+    (one extra rounding apart); deterministic run to run."""
+    w = SMALL[name]
+    cfg = api.config_for(w)
+    inp = synth.make_inputs(w, seed=4, device="cpu")
+    a = run_forward(cfg, gpu_inputs(inp))
+    b = run_forward(cfg, gpu_inputs(inp))
+    assert torch.equal(a["out"], b["out"])
+    s = run_staged(cfg, gpu_inputs(inp))
+    assert torch.equal(a["idx"], s["idx"]) and torch.equal(a["gate"], s["gate"])
+    fa, fs = np_f(a["out"]), np_f(s["out"])
+    assert (np.abs(fa - fs) <= 2.0 ** -7 * np.abs(fs) + 1e-6).all()
+    o = oracle_inputs(inp)
+    out_ref, mag = reference_layer(w, o, np_i(a["idx"]))
+    assert_layer_close(fa, out_ref, mag, out_tol(w), f"{name} fused top-1")

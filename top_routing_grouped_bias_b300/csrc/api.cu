@@ -83,7 +83,9 @@ moe_status dispatch_impl(const moe_config* cfg, const void* h, const int32_t* id
 moe_status ffn_impl(const moe_config* cfg, const void* x_disp, const int32_t* offsets,
                     const void* W_gate, const void* W_up, const void* W_down, void* y_rows,
                     const void* h, const void* Ws_gate, const void* Ws_up, const void* Ws_down,
-                    void* y_shared, void* ws, const WsLayout& L, cudaStream_t stream) {
+                    void* y_shared, void* ws, const WsLayout& L, cudaStream_t stream,
+                    const int32_t* scatter_token = nullptr, const float* scatter_gate = nullptr,
+                    void* scatter_out = nullptr) {
   if (!ok_tensor(x_disp) || !ok_f32(offsets) || !ok_tensor(W_gate) || !ok_tensor(W_up) ||
       !ok_tensor(W_down) || !ok_tensor(y_rows))
     return MOE_ERR_INVALID_ARG;
@@ -98,6 +100,9 @@ moe_status ffn_impl(const moe_config* cfg, const void* x_disp, const int32_t* of
   a.status = at<int32_t>(ws, L.status);
   a.T = cfg->T; a.d = cfg->d; a.N = cfg->N; a.k = cfg->k; a.F = cfg->ffn; a.F_sh = cfg->ffn_shared;
   a.dtype = cfg->dtype;
+  a.scatter_token = scatter_token;
+  a.scatter_gate = scatter_gate;
+  a.scatter_out = scatter_out;
   return from_cuda(launch_expert_ffn(a, stream));
 }
 
@@ -199,6 +204,18 @@ moe_status forward_impl(const moe_config* cfg, int64_t capacity, const void* h, 
   if (s != MOE_OK) return s;
   s = dispatch_impl(cfg, h, idx, cnt, offsets, row_token, inv, x_disp, ws, L, stream, capacity);
   if (s != MOE_OK) return s;
+  // top-1 without a shared expert: out[t] = g_t * E(h_t) is written by the
+  // down pass itself (one scaled store per row, no y_rows round trip);
+  // tokens whose only pair was dropped (capacity) are cleared first
+  const bool fuse = cfg->k == 1 && cfg->ffn_shared == 0;
+  if (fuse) {
+    if (capacity >= 0) {
+      const size_t bytes = static_cast<size_t>(cfg->T) * cfg->d * elem_size(cfg->dtype);
+      if (cudaMemsetAsync(out, 0, bytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return ffn_impl(cfg, x_disp, offsets, W_gate, W_up, W_down, y_rows, h, Ws_gate, Ws_up,
+                    Ws_down, y_sh, ws, L, stream, row_token, gate, out);
+  }
   s = ffn_impl(cfg, x_disp, offsets, W_gate, W_up, W_down, y_rows, h, Ws_gate, Ws_up, Ws_down,
                y_sh, ws, L, stream);
   if (s != MOE_OK) return s;

@@ -95,6 +95,11 @@ struct GemmParams {
   int32_t* status;
   uint64_t budget_ns;
   RouteEpi re;
+  // Down pass with top-1 routing and no shared expert: the combine is a
+  // scaled scatter, so the epilogue writes gate * y to the token's output row
+  // (out = [T, n_out]) instead of writing y_rows. Null: plain y_rows.
+  const int32_t* scatter_token;  // dispatched row -> token
+  const float* scatter_gate;     // [T] gate of each token's single slot
 };
 
 struct TileInfo {
@@ -529,6 +534,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool dense = ti.g >= p.n_routed;
       T* out = dense ? static_cast<T*>(p.out_shared) + static_cast<size_t>(row) * p.n_out_shared
                      : static_cast<T*>(p.out) + static_cast<size_t>(ti.row0 + row) * p.n_out;
+      float scale = 1.f;
+      if (MODE == kDown && p.scatter_token != nullptr && !dense && row_ok) {
+        const int tok = p.scatter_token[ti.row0 + row];
+        scale = p.scatter_gate[tok];
+        out = static_cast<T*>(p.out) + static_cast<size_t>(tok) * p.n_out;
+      }
       out += col0;
       if (MODE == kRoute) {
         route_epilogue<KT>(tbase, row, row_ok, p.n_out, p.re);
@@ -557,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (row_ok && c < cols_left) {
             float f[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]) * scale;
             store32(out + c, f, cols_left - c);
           }
         }
@@ -805,6 +816,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool dense = ti.g >= p.n_routed;
       T* out = dense ? static_cast<T*>(p.out_shared) + static_cast<size_t>(row) * p.n_out_shared
                      : static_cast<T*>(p.out) + static_cast<size_t>(ti.row0 + row) * p.n_out;
+      float scale = 1.f;
+      if (MODE == kDown && p.scatter_token != nullptr && !dense && row_ok) {
+        const int tok = p.scatter_token[ti.row0 + row];
+        scale = p.scatter_gate[tok];
+        out = static_cast<T*>(p.out) + static_cast<size_t>(tok) * p.n_out;
+      }
       out += col0;
       if (MODE == kSwiGLU) {
 #pragma unroll 1
@@ -831,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (row_ok && c < cols_left) {
             float f[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]) * scale;
             store32(out + c, f, cols_left - c);
           }
         }
@@ -1037,11 +1054,13 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
     m[3] = m[0]; m[4] = m[1]; m[5] = m[1];
   }
   GemmParams pb = pa;
+  pb.scatter_token = a.scatter_token;
+  pb.scatter_gate = a.scatter_gate;
   pb.K = a.F;
   pb.K_shared = a.F_sh;
   pb.n_out = a.d;
   pb.n_out_shared = a.d;
-  pb.out = a.y_rows;
+  pb.out = a.scatter_token != nullptr ? a.scatter_out : a.y_rows;
   pb.out_shared = a.y_shared;
   if (pair) return launch_gemm_pair<kDown>(m, pb, tiles_bound(R, a.N, a.d, 256, sh ? a.T : 0, a.d, 256),
                                            stream);

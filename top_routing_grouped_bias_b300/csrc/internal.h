@@ -116,6 +116,10 @@ struct FfnArgs {
   int64_t T;
   int32_t d, N, k, F, F_sh, dtype;
   int64_t rows;  // dispatched rows when not T*k (0 = T*k)
+  // top-1 without a shared expert: fuse the combine into the down pass
+  const int32_t* scatter_token;  // row -> token, or null
+  const float* scatter_gate;     // [T]
+  void* scatter_out;             // [T, d]
 };
 cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream);
 
