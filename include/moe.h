@@ -183,6 +183,20 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_disp,
                           const void* Ws_down, void* y_shared,
                           void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* moe_expert_ffn with the routed rows read straight from h: dispatched row r
+ * is h[row_token[r]] (the row_token of moe_dispatch, which can then skip its
+ * x_disp copy). The gate/up pass fetches each 128-row tile with TMA gather4
+ * loads, four rows per instruction. bf16 only (MOE_ERR_UNSUPPORTED for fp32).
+ * It saves the [T*k, d] dispatched copy (memory and its HBM round trip) but
+ * issues 32 gather loads per pipeline stage instead of one 16 KB box, which
+ * made the grouped GEMM ~2.5x slower on B300; moe_forward uses the copy.
+ * Otherwise as moe_expert_ffn. */
+moe_status moe_expert_ffn_gather(const moe_config* cfg, const void* h, const int32_t* row_token,
+                                 const int32_t* offsets, const void* W_gate, const void* W_up,
+                                 const void* W_down, void* y_rows, const void* Ws_gate,
+                                 const void* Ws_up, const void* Ws_down, void* y_shared, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream);
+
 /* Stage 7: weighted scatter-ADD of every expert output back to its token.
  * [P2] 选好以后: outputs are added, never overwritten or concatenated;
  * [P5] §3 ④ Gather; [P1] §八 shared-expert term.

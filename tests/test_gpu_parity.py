@@ -349,3 +349,25 @@ def test_fused_top1_forward_vs_oracle(cuda_lib, name):
     o = oracle_inputs(inp)
     out_ref, mag = reference_layer(w, o, np_i(a["idx"]))
     assert_layer_close(fa, out_ref, mag, out_tol(w), f"{name} fused top-1")
+
+
+@pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "many_experts",
+                                  "pair_shared_ragged_n", "multi_mtile_ragged_n"])
+def test_gather_ffn_equals_dispatched_copy(cuda_lib, name):
+    """The grouped GEMM fed by TMA gather4 from h (the moe_forward path) gives
+    bitwise the same rows as the one fed by the dispatched copy x_disp."""
+    w = SMALL[name]
+    cfg = api.config_for(w)
+    inp = gpu_inputs(synth.make_inputs(w, seed=11, device="cpu"))
+    r = run_staged(cfg, inp)
+    ws = api.alloc_workspace(cfg, "cuda")
+    y = torch.empty_like(r["y_rows"])
+    ysh = torch.empty_like(r["y_sh"]) if w.F_sh else None
+    api.moe_expert_ffn_gather(cfg, inp["h"], r["row_token"], r["offsets"], inp["W_gate"],
+                              inp["W_up"], inp["W_down"], y, inp.get("Ws_gate"), inp.get("Ws_up"),
+                              inp.get("Ws_down"), ysh, ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    assert torch.equal(y, r["y_rows"])
+    if w.F_sh:
+        assert torch.equal(ysh, r["y_sh"])

@@ -33,7 +33,7 @@ ENTRY_POINTS = (
     "moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
     "moe_forward", "moe_read_status", "moe_selftest_wait_timeout", "moe_status_string",
     "moe_dispatch_noalloc", "moe_route_stats", "moe_route_grouped", "moe_dispatch_capacity",
-    "moe_forward_capacity", "moe_forward_expert_choice",
+    "moe_forward_capacity", "moe_forward_expert_choice", "moe_expert_ffn_gather",
 )
 
 
@@ -88,6 +88,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_route_grouped.argtypes = [cfgp, ctypes.POINTER(MoeGroupConfig)] + [_vp] * 8 + \
         [_vp, _sz, _vp]
     lib.moe_expert_ffn.argtypes = [cfgp] + [_vp] * 11 + [_vp, _sz, _vp]
+    lib.moe_expert_ffn_gather.argtypes = [cfgp] + [_vp] * 11 + [_vp, _sz, _vp]
     lib.moe_combine.argtypes = [cfgp] + [_vp] * 5 + [_vp]
     lib.moe_forward.argtypes = [cfgp] + [_vp] * 15 + [_vp, _sz, _vp]
     lib.moe_read_status.argtypes = [_vp, _sz, _i32p, _vp]
@@ -178,6 +179,16 @@ def moe_expert_ffn(cfg, x_disp, offsets, W_gate, W_up, W_down, y_rows, h=None, W
                               _p(y_shared), _p(ws), 0 if ws is None else ws.numel(),
                               _stream(stream))
     _check(s, "moe_expert_ffn")
+
+
+def moe_expert_ffn_gather(cfg, h, row_token, offsets, W_gate, W_up, W_down, y_rows,
+                          Ws_gate=None, Ws_up=None, Ws_down=None, y_shared=None, ws=None,
+                          stream=None):
+    s = load().moe_expert_ffn_gather(ctypes.byref(cfg), _p(h), _p(row_token), _p(offsets),
+                                     _p(W_gate), _p(W_up), _p(W_down), _p(y_rows), _p(Ws_gate),
+                                     _p(Ws_up), _p(Ws_down), _p(y_shared), _p(ws),
+                                     0 if ws is None else ws.numel(), _stream(stream))
+    _check(s, "moe_expert_ffn_gather")
 
 
 def moe_combine(cfg, y_rows, inv, gate, y_shared, out, stream=None):

@@ -85,8 +85,9 @@ moe_status ffn_impl(const moe_config* cfg, const void* x_disp, const int32_t* of
                     const void* h, const void* Ws_gate, const void* Ws_up, const void* Ws_down,
                     void* y_shared, void* ws, const WsLayout& L, cudaStream_t stream,
                     const int32_t* scatter_token = nullptr, const float* scatter_gate = nullptr,
-                    void* scatter_out = nullptr) {
-  if (!ok_tensor(x_disp) || !ok_f32(offsets) || !ok_tensor(W_gate) || !ok_tensor(W_up) ||
+                    void* scatter_out = nullptr, const int32_t* gather_rows = nullptr) {
+  const bool a_ok = gather_rows != nullptr ? ok_tensor(h) && ok_f32(gather_rows) : ok_tensor(x_disp);
+  if (!a_ok || !ok_f32(offsets) || !ok_tensor(W_gate) || !ok_tensor(W_up) ||
       !ok_tensor(W_down) || !ok_tensor(y_rows))
     return MOE_ERR_INVALID_ARG;
   if (cfg->ffn_shared > 0 && (!ok_tensor(h) || !ok_tensor(Ws_gate) || !ok_tensor(Ws_up) ||
@@ -103,6 +104,7 @@ moe_status ffn_impl(const moe_config* cfg, const void* x_disp, const int32_t* of
   a.scatter_token = scatter_token;
   a.scatter_gate = scatter_gate;
   a.scatter_out = scatter_out;
+  a.gather_rows = gather_rows;
   return from_cuda(launch_expert_ffn(a, stream));
 }
 
@@ -165,6 +167,21 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_disp, const int32
                   y_shared, ws, L, stream);
 }
 
+moe_status moe_expert_ffn_gather(const moe_config* cfg, const void* h, const int32_t* row_token,
+                                 const int32_t* offsets, const void* W_gate, const void* W_up,
+                                 const void* W_down, void* y_rows, const void* Ws_gate,
+                                 const void* Ws_up, const void* Ws_down, void* y_shared, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (row_token == nullptr) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  if (!ws_ok(ws, ws_bytes, L.end_ffn)) return MOE_ERR_WORKSPACE;
+  return ffn_impl(cfg, nullptr, offsets, W_gate, W_up, W_down, y_rows, h, Ws_gate, Ws_up, Ws_down,
+                  y_shared, ws, L, stream, nullptr, nullptr, nullptr, row_token);
+}
+
 moe_status moe_combine(const moe_config* cfg, const void* y_rows, const int32_t* inv,
                        const float* gate, const void* y_shared, void* out, cudaStream_t stream) {
   moe_status s = check_config(cfg);
@@ -202,6 +219,10 @@ moe_status forward_impl(const moe_config* cfg, int64_t capacity, const void* h, 
   s = route_impl(cfg, h, W_r, b_r, sel_bias, nullptr, logits_out, idx, gate,
                  at<int32_t>(ws, L.status), stream);
   if (s != MOE_OK) return s;
+  // The dispatched copy feeds the gate/up pass with one 16 KB TMA box per
+  // stage; reading the rows from h by index (gather4, moe_expert_ffn_gather)
+  // saves the copy but issues 32 loads per stage and runs ~2.5x slower.
+  const int32_t* gather = nullptr;
   s = dispatch_impl(cfg, h, idx, cnt, offsets, row_token, inv, x_disp, ws, L, stream, capacity);
   if (s != MOE_OK) return s;
   // top-1 without a shared expert: out[t] = g_t * E(h_t) is written by the
@@ -214,10 +235,10 @@ moe_status forward_impl(const moe_config* cfg, int64_t capacity, const void* h, 
       if (cudaMemsetAsync(out, 0, bytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
     }
     return ffn_impl(cfg, x_disp, offsets, W_gate, W_up, W_down, y_rows, h, Ws_gate, Ws_up,
-                    Ws_down, y_sh, ws, L, stream, row_token, gate, out);
+                    Ws_down, y_sh, ws, L, stream, row_token, gate, out, gather);
   }
   s = ffn_impl(cfg, x_disp, offsets, W_gate, W_up, W_down, y_rows, h, Ws_gate, Ws_up, Ws_down,
-               y_sh, ws, L, stream);
+               y_sh, ws, L, stream, nullptr, nullptr, nullptr, gather);
   if (s != MOE_OK) return s;
   return combine_impl(cfg, y_rows, inv, gate, y_sh, out, stream);
 }

@@ -100,6 +100,10 @@ struct GemmParams {
   // (out = [T, n_out]) instead of writing y_rows. Null: plain y_rows.
   const int32_t* scatter_token;  // dispatched row -> token
   const float* scatter_gate;     // [T] gate of each token's single slot
+  // Gate/up pass reading the routed rows straight from h: A0 is then h with
+  // a 1-row box and dispatched row r is h[gather_rows[r]] (TMA gather4).
+  // Null: A0 is the dispatched copy x_disp.
+  const int32_t* gather_rows;
 };
 
 struct TileInfo {
@@ -420,28 +424,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, issued_mask = 0, issued_par = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
-        const bool dense = ti.g >= p.n_routed;
-        const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
-        const void* mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
-        const void* mBu = dense ? static_cast<const void*>(&mapB1u) : static_cast<const void*>(&mapB0u);
-        const int a_row = ti.row0 + ti.m_blk * kBM;
-        const int b_row = ti.b_row0 + ti.n_blk * BN;
-        for (int kb = 0; kb < ti.num_kb; ++kb) {
-          if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_v, p.status, p.budget_ns,
-                                 MOE_ERR_TIMEOUT)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sA = smem + stage * kStageBytes;
-          uint8_t* sB = sA + kStageA;
-          mbar_arrive_expect_tx(&full_bar[stage], stage_tx);
-          tma_load_2d(sA, mA, &full_bar[stage], kb * BK, a_row);
+    // Lane 0 waits for free stages, arms the barriers and issues the tiled
+    // loads; when the routed rows come from h by index, every lane issues one
+    // gather4 (4 of the tile's 128 rows) per stage.
+    int stage = 0;
+    uint32_t phase = 0, issued_mask = 0, issued_par = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const TileInfo ti = decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+      const bool dense = ti.g >= p.n_routed;
+      const bool gather = MODE == kSwiGLU && p.gather_rows != nullptr && !dense;
+      const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
+      const void* mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
+      const void* mBu = dense ? static_cast<const void*>(&mapB1u) : static_cast<const void*>(&mapB0u);
+      const int a_row = ti.row0 + ti.m_blk * kBM;
+      const int b_row = ti.b_row0 + ti.n_blk * BN;
+      int g4[4] = {0, 0, 0, 0};
+      if (gather) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          // rows past the routed rows repeat the last one (their results are masked)
+          const int r = min(a_row + lane * 4 + i, grp_off[p.n_routed] - 1);
+          g4[i] = p.gather_rows[r];
+        }
+      }
+      for (int kb = 0; kb < ti.num_kb; ++kb) {
+        bool w = true;
+        if (lane == 0) {
+          w = mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_v, p.status, p.budget_ns,
+                                MOE_ERR_TIMEOUT);
+          if (w) mbar_arrive_expect_tx(&full_bar[stage], stage_tx);
+        }
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        uint8_t* sA = smem + stage * kStageBytes;
+        uint8_t* sB = sA + kStageA;
+        if (gather) tma_gather4(sA + lane * 512, mA, &full_bar[stage], kb * BK, g4[0], g4[1], g4[2], g4[3]);
+        if (lane == 0) {
+          if (!gather) tma_load_2d(sA, mA, &full_bar[stage], kb * BK, a_row);
           if (MODE == kSwiGLU) {
             tma_load_2d(sB, mB, &full_bar[stage], kb * BK, b_row);
             tma_load_2d(sB + kStageB / 2, mBu, &full_bar[stage], kb * BK, b_row);
@@ -450,16 +473,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      if (!ok) {
-        for (int s = 0; s < kStages; ++s)
-          if ((issued_mask >> s) & 1u) drain_wait(&full_bar[s], (issued_par >> s) & 1u);
-      }
+    }
+    if (!ok && lane == 0) {
+      for (int s = 0; s < kStages; ++s)
+        if ((issued_mask >> s) & 1u) drain_wait(&full_bar[s], (issued_par >> s) & 1u);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -700,49 +723,65 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
-        const TileInfo ti = decode_tile<BN, BK, BM>(tile, tile_start, grp_off, G, p);
-        const bool dense = ti.g >= p.n_routed;
-        const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
-        const void* mB;
-        int b_row;
-        if (MODE == kSwiGLU) {
-          // CTA 0 holds the W_gate half of B, CTA 1 the W_up half
-          mB = leader ? (dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0))
-                      : (dense ? static_cast<const void*>(&mapB1u) : static_cast<const void*>(&mapB0u));
-          b_row = ti.b_row0 + ti.n_blk * BN;
-        } else {
-          mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
-          b_row = ti.b_row0 + ti.n_blk * BN + static_cast<int>(rank) * 128;
-        }
-        const int a_row = ti.row0 + ti.m_blk * BM + static_cast<int>(rank) * 128;
-        for (int kb = 0; kb < ti.num_kb; ++kb) {
-          if (!mbar_wait_bounded_cluster(&empty_bar[stage], phase ^ 1u, abort_v, p.status,
-                                         p.budget_ns, MOE_ERR_TIMEOUT)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sA = smem + stage * kPairStageBytes;
-          uint8_t* sB = sA + kPairStageA;
-          const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
-          tma_load_2d_pair(sA, mA, full_leader, kb * BK, a_row);
-          tma_load_2d_pair(sB, mB, full_leader, kb * BK, b_row);
-          if (++stage == kPairStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
+      const TileInfo ti = decode_tile<BN, BK, BM>(tile, tile_start, grp_off, G, p);
+      const bool dense = ti.g >= p.n_routed;
+      const bool gather = MODE == kSwiGLU && p.gather_rows != nullptr && !dense;
+      const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
+      const void* mB;
+      int b_row;
+      if (MODE == kSwiGLU) {
+        // CTA 0 holds the W_gate half of B, CTA 1 the W_up half
+        mB = leader ? (dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0))
+                    : (dense ? static_cast<const void*>(&mapB1u) : static_cast<const void*>(&mapB0u));
+        b_row = ti.b_row0 + ti.n_blk * BN;
+      } else {
+        mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
+        b_row = ti.b_row0 + ti.n_blk * BN + static_cast<int>(rank) * 128;
+      }
+      const int a_row = ti.row0 + ti.m_blk * BM + static_cast<int>(rank) * 128;
+      int g4[4] = {0, 0, 0, 0};
+      if (gather) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = min(a_row + lane * 4 + i, grp_off[p.n_routed] - 1);
+          g4[i] = p.gather_rows[r];
         }
       }
-      if (!ok) {
-        // let loads already issued land before the CTA can leave
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 2000000ull) {
+      for (int kb = 0; kb < ti.num_kb; ++kb) {
+        bool w = true;
+        if (lane == 0)
+          w = mbar_wait_bounded_cluster(&empty_bar[stage], phase ^ 1u, abort_v, p.status,
+                                        p.budget_ns, MOE_ERR_TIMEOUT);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) {
+          ok = false;
+          break;
         }
+        uint8_t* sA = smem + stage * kPairStageBytes;
+        uint8_t* sB = sA + kPairStageA;
+        const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[stage]), 0);
+        if (lane == 0 && leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
+        __syncwarp();
+        if (gather)
+          tma_gather4_pair(sA + lane * 512, mA, full_leader, kb * BK, g4[0], g4[1], g4[2], g4[3]);
+        if (lane == 0) {
+          if (!gather) tma_load_2d_pair(sA, mA, full_leader, kb * BK, a_row);
+          tma_load_2d_pair(sB, mB, full_leader, kb * BK, b_row);
+        }
+        if (++stage == kPairStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // let loads already issued land before the CTA can leave
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 2000000ull) {
       }
     }
   } else if (warp == 1) {
@@ -1000,8 +1039,14 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   const int sms = num_sms();
   CUtensorMap m[6];
 
-  // pass A: act = SiLU(x Wg^T) * (x Wu^T)
-  if (!make_map(&m[0], a.x_disp, a.dtype, a.d, R, kBM)) return cudaErrorInvalidValue;
+  // pass A: act = SiLU(x Wg^T) * (x Wu^T); x is the dispatched copy, or the
+  // rows of h picked by index (gather4, 1-row box) when gather_rows is given
+  const bool gather = a.gather_rows != nullptr;
+  if (gather) {
+    if (!make_map(&m[0], a.h, a.dtype, a.d, a.T, 1)) return cudaErrorInvalidValue;
+  } else if (!make_map(&m[0], a.x_disp, a.dtype, a.d, R, kBM)) {
+    return cudaErrorInvalidValue;
+  }
   if (!make_map(&m[1], a.W_gate, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, 128)) return cudaErrorInvalidValue;
   if (!make_map(&m[2], a.W_up, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, 128)) return cudaErrorInvalidValue;
   if (sh) {
@@ -1024,6 +1069,7 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   pa.out_shared = a.act_sh;
   pa.status = a.status;
   pa.budget_ns = kWaitBudgetNs;
+  pa.gather_rows = a.gather_rows;
   // CTA pairs (256-row tiles) pay off when experts hold many rows on average;
   // with few rows per expert the 128-row tiles waste less of the MMA.
   const bool pair = a.dtype == MOE_BF16 && R >= static_cast<int64_t>(kPairMinRowsPerExpert) * a.N;
@@ -1054,6 +1100,7 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
     m[3] = m[0]; m[4] = m[1]; m[5] = m[1];
   }
   GemmParams pb = pa;
+  pb.gather_rows = nullptr;
   pb.scatter_token = a.scatter_token;
   pb.scatter_gate = a.scatter_gate;
   pb.K = a.F;

@@ -120,6 +120,8 @@ struct FfnArgs {
   const int32_t* scatter_token;  // row -> token, or null
   const float* scatter_gate;     // [T]
   void* scatter_out;             // [T, d]
+  // gate/up A operand straight from h by dispatched-row index (no x_disp)
+  const int32_t* gather_rows;    // row -> token, or null
 };
 cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream);
 

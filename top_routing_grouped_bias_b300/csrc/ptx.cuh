@@ -291,3 +291,31 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
 }
 
 }  // namespace moe
+
+namespace moe {
+// Four rows of a 2-D tensor, at arbitrary row coordinates, one 128-byte
+// column slice each (the tensor map's box is 1 row high), written as four
+// consecutive 128-byte rows at `smem_dst` with the map's swizzle.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* map, uint64_t* bar,
+                                            int32_t x, int32_t y0, int32_t y1, int32_t y2,
+                                            int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2),
+      "r"(y3)
+      : "memory");
+}
+
+// Same into a CTA pair's shared memory, completion on the pair barrier.
+__device__ __forceinline__ void tma_gather4_pair(void* smem_dst, const void* map,
+                                                 uint32_t mbar_cluster, int32_t x, int32_t y0,
+                                                 int32_t y1, int32_t y2, int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster), "r"(x), "r"(y0), "r"(y1), "r"(y2),
+      "r"(y3)
+      : "memory");
+}
+}  // namespace moe
