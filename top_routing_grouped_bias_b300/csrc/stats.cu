@@ -93,17 +93,33 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
   }
   __syncthreads();
   float* P = a.partial + static_cast<size_t>(blockIdx.x) * (2 * N + 2);
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+  // per-expert probability sums: with few experts several threads share an
+  // expert, each summing every ns-th token in order; the slices are then
+  // added in slice order (fixed order, deterministic)
+  const int ns = N >= 256 ? 1 : (256 / N < 32 ? 256 / N : 32);
+  __shared__ float s_part[256];
+  for (int e0 = 0; e0 < N; e0 += 256 / ns) {
+    const int e = e0 + threadIdx.x % (256 / ns);
+    const int sl = threadIdx.x / (256 / ns);
     float acc = 0.f;
-    for (int lt = 0; lt < kTok; ++lt) {
-      const int64_t t = t0 + lt;
-      if (t >= a.T) break;
-      const float z = a.logits[t * N + e];
-      acc += softmax ? expf(z - s_m[lt]) / s_norm[lt] : 1.f / (1.f + expf(-z)) / s_norm[lt];
+    if (e < N && sl < ns) {
+      for (int lt = sl; lt < kTok; lt += ns) {
+        const int64_t t = t0 + lt;
+        if (t >= a.T) break;
+        const float z = a.logits[t * N + e];
+        acc += softmax ? expf(z - s_m[lt]) / s_norm[lt] : 1.f / (1.f + expf(-z)) / s_norm[lt];
+      }
     }
-    P[e] = acc;
-    P[N + e] = static_cast<float>(s_cnt[e]);
+    s_part[threadIdx.x] = acc;
+    __syncthreads();
+    if (threadIdx.x < 256 / ns && e0 + static_cast<int>(threadIdx.x) < N) {
+      float tot = 0.f;
+      for (int q = 0; q < ns; ++q) tot += s_part[q * (256 / ns) + threadIdx.x];
+      P[e0 + threadIdx.x] = tot;
+    }
+    __syncthreads();
   }
+  for (int e = threadIdx.x; e < N; e += blockDim.x) P[N + e] = static_cast<float>(s_cnt[e]);
   if (threadIdx.x == 0) {
     float l2 = 0.f, en = 0.f;
     for (int lt = 0; lt < kTok; ++lt) {
