@@ -42,6 +42,15 @@ SMALL = {
     "pair_ragged": Workload("pair_ragged", T=1700, d=256, N=2, F=384, k=1),
     "pair_shared_ragged_n": Workload("pair_shared_ragged_n", T=2100, d=192, N=2, F=320, k=1,
                                      F_sh=256, score="sigmoid", bias_zipf_s=1.1),
+    # CTA pairs with 128-row half tiles: expert counts [3203, 48, 23, 126] (one
+    # full 256-row tail, three groups that are a single half tile) and a dense
+    # group of 3400 rows whose tail has 72 rows; ragged n (F=448, d=320)
+    "pair_half_tails": Workload("pair_half_tails", T=3400, d=320, N=4, F=448, k=1, F_sh=192,
+                                bias_zipf_s=1.1, bias_beta=0.4),
+    # counts [1640, 546, 499, 715]: tails of 104 and 34 rows (half) and 243
+    # and 203 rows (full) behind several full m-tiles
+    "pair_mixed_tails": Workload("pair_mixed_tails", T=3400, d=256, N=4, F=384, k=1,
+                                 score="sigmoid", bias_zipf_s=1.1, bias_beta=0.1),
 }
 
 
@@ -118,7 +127,7 @@ def test_small_workload_stagewise_parity(cuda_lib, name):
 
 
 @pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "tiny_fp32",
-                                  "many_experts", "pair_shared_ragged_n"])
+                                  "many_experts", "pair_shared_ragged_n", "pair_half_tails"])
 def test_forward_equals_stages_and_is_deterministic(cuda_lib, name):
     w = SMALL[name]
     cfg = api.config_for(w)
@@ -331,7 +340,7 @@ def test_route_tensor_core_exact_ties(cuda_lib, score, N, k):
     assert (np.abs(z - O.router_logits(to_f64(h), to_f64(W))) <= bound).all()
 
 
-@pytest.mark.parametrize("name", ["switch_top1", "one_expert", "pair_ragged"])
+@pytest.mark.parametrize("name", ["switch_top1", "one_expert", "pair_ragged", "pair_mixed_tails"])
 def test_fused_top1_forward_vs_oracle(cuda_lib, name):
     """Top-1 without a shared expert: moe_forward writes g * E(h) from the down
     pass directly. Checked against the oracle and against the staged path
@@ -352,7 +361,8 @@ def test_fused_top1_forward_vs_oracle(cuda_lib, name):
 
 
 @pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "many_experts",
-                                  "pair_shared_ragged_n", "multi_mtile_ragged_n"])
+                                  "pair_shared_ragged_n", "multi_mtile_ragged_n", "pair_half_tails",
+                                  "pair_mixed_tails"])
 def test_gather_ffn_equals_dispatched_copy(cuda_lib, name):
     """The grouped GEMM fed by TMA gather4 from h (the moe_forward path) gives
     bitwise the same rows as the one fed by the dispatched copy x_disp."""
@@ -371,3 +381,15 @@ def test_gather_ffn_equals_dispatched_copy(cuda_lib, name):
     assert torch.equal(y, r["y_rows"])
     if w.F_sh:
         assert torch.equal(ysh, r["y_sh"])
+
+
+@pytest.mark.parametrize("name", ["pair_half_tails", "pair_mixed_tails"])
+def test_pair_workloads_cover_both_tail_kinds(cuda_lib, name):
+    """The two pair workloads above must keep exercising what they were chosen
+    for: group tails of 1..128 rows (half tiles) and of 129..255 rows."""
+    w = SMALL[name]
+    r = run_staged(api.config_for(w), gpu_inputs(synth.make_inputs(w, seed=0, device="cpu")))
+    c = np_i(r["counts"])
+    assert c.sum() >= 768 * w.N, "the grouped GEMM would not run on CTA pairs"
+    rem = c % 256
+    assert ((rem >= 1) & (rem <= 128)).any() and (rem > 128).any(), c.tolist()
