@@ -42,13 +42,13 @@ SMALL = {
     "pair_ragged": Workload("pair_ragged", T=1700, d=256, N=2, F=384, k=1),
     "pair_shared_ragged_n": Workload("pair_shared_ragged_n", T=2100, d=192, N=2, F=320, k=1,
                                      F_sh=256, score="sigmoid", bias_zipf_s=1.1),
-    # CTA pairs with 128-row half tiles: expert counts [3203, 48, 23, 126] (one
-    # full 256-row tail, three groups that are a single half tile) and a dense
-    # group of 3400 rows whose tail has 72 rows; ragged n (F=448, d=320)
+    # CTA pairs, expert counts [3203, 48, 23, 126]: one 131-row tail behind
+    # twelve full m-tiles, three groups that are a single masked tile, and a
+    # dense group of 3400 rows whose tail has 72 rows; ragged n (F=448, d=320)
     "pair_half_tails": Workload("pair_half_tails", T=3400, d=320, N=4, F=448, k=1, F_sh=192,
                                 bias_zipf_s=1.1, bias_beta=0.4),
-    # counts [1640, 546, 499, 715]: tails of 104 and 34 rows (half) and 243
-    # and 203 rows (full) behind several full m-tiles
+    # counts [1640, 546, 499, 715]: masked tails of 104, 34, 243 and 203 rows
+    # behind several full m-tiles
     "pair_mixed_tails": Workload("pair_mixed_tails", T=3400, d=256, N=4, F=384, k=1,
                                  score="sigmoid", bias_zipf_s=1.1, bias_beta=0.1),
 }
@@ -386,7 +386,8 @@ def test_gather_ffn_equals_dispatched_copy(cuda_lib, name):
 @pytest.mark.parametrize("name", ["pair_half_tails", "pair_mixed_tails"])
 def test_pair_workloads_cover_both_tail_kinds(cuda_lib, name):
     """The two pair workloads above must keep exercising what they were chosen
-    for: group tails of 1..128 rows (half tiles) and of 129..255 rows."""
+    for: masked group tails of 1..128 rows (one CTA of the pair holds no valid
+    row) and of 129..255 rows."""
     w = SMALL[name]
     r = run_staged(api.config_for(w), gpu_inputs(synth.make_inputs(w, seed=0, device="cpu")))
     c = np_i(r["counts"])

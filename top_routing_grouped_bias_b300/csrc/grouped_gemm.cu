@@ -616,24 +616,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // CTA-pair variant (tcgen05.mma.cta_group::2): a cluster of two CTAs on two SMs
 // computes one 256-row tile. Each CTA loads its own 128 rows of A and one half
-// of the 256-row B tile, so each SM fetches 32 KB per K-step instead of 48 KB
-// for the same tensor-core work. The leader CTA (rank 0) issues the MMAs for
-// the pair; both CTAs' TMA loads count on the leader's full barrier, the
-// leader's commits arrive on both CTAs' empty and accumulator-full barriers,
-// and both CTAs' epilogue threads arrive on the leader's accumulator-empty
-// barrier.
-//
-// B halves. Pass B: CTA r holds W_down rows [n0 + 128 r, +128). Pass A: CTA r
-// holds W_gate rows [j + 64 r, +64) over W_up rows [j + 64 r, +64) of a
-// 128-column output tile starting at j, so every accumulator row keeps the
-// gate and up values of one output column within one 128-column half.
-//
-// Half tiles. The last m-tile of a group with at most 128 rows left runs as an
-// M=128 pair MMA (64 A rows per CTA, A box 64 rows), half the tensor work of a
-// padded 256-row tile. Its accumulator, per CTA: TMEM lanes 0..63 hold the
-// CTA's 64 rows for MMA columns 0..127 (CTA 0's B half) and lanes 64..127 the
-// same rows for columns 128..255 (CTA 1's B half), both in TMEM columns 0..127.
-// A full tile: lanes 0..127 hold the CTA's 128 rows, TMEM columns 0..255.
+// of the 256-row B tile (pass A: CTA 0 the W_gate rows, CTA 1 the W_up rows;
+// pass B: one 128-row half of W_down each), so each SM fetches 32 KB per
+// K-step instead of 48 KB for the same tensor-core work. The leader CTA (rank
+// 0) issues the MMAs for the pair; both CTAs' TMA loads count on the leader's
+// full barrier, the leader's commits arrive on both CTAs' empty and
+// accumulator-full barriers, and both CTAs' epilogue threads arrive on the
+// leader's accumulator-empty barrier. Each CTA drains its own 128 TMEM lanes.
 constexpr int kPairStages = MOE_PAIR_STAGES;
 constexpr uint32_t kPairStageA = 128 * 128;
 constexpr uint32_t kPairStageB = 128 * 128;
@@ -647,15 +636,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap mapB0u,
                              const __grid_constant__ CUtensorMap mapA1,
                              const __grid_constant__ CUtensorMap mapB1,
-                             const __grid_constant__ CUtensorMap mapB1u,
-                             const __grid_constant__ CUtensorMap mapA0h,
-                             const __grid_constant__ CUtensorMap mapA1h, const GemmParams p) {
+                             const __grid_constant__ CUtensorMap mapB1u, const GemmParams p) {
   using T = __nv_bfloat16;
   constexpr int BK = 64;
   constexpr int BM = 256;                                  // rows per pair tile
   constexpr int BN = MODE == kSwiGLU ? 128 : 256;
-  const uint32_t idesc_full = make_idesc(BM, 256, 1u);
-  const uint32_t idesc_half = make_idesc(BM / 2, 256, 1u);
+  const uint32_t idesc = make_idesc(BM, 256, 1u);
 
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -744,16 +730,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo ti = decode_tile<BN, BK, BM>(tile, tile_start, grp_off, G, p);
       const bool dense = ti.g >= p.n_routed;
       const bool gather = MODE == kSwiGLU && p.gather_rows != nullptr && !dense;
-      const bool half = ti.rows - ti.m_blk * BM <= BM / 2;
-      const void* mA = dense ? (half ? static_cast<const void*>(&mapA1h) : static_cast<const void*>(&mapA1))
-                             : (half ? static_cast<const void*>(&mapA0h) : static_cast<const void*>(&mapA0));
-      const void* mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
-      const void* mBu = dense ? static_cast<const void*>(&mapB1u) : static_cast<const void*>(&mapB0u);
-      // pass A: W_gate / W_up rows [j + 64 rank, +64); pass B: W_down rows [n0 + 128 rank, +128)
-      const int b_row = ti.b_row0 + ti.n_blk * BN + static_cast<int>(rank) * (BN / 2);
-      const int a_rows = half ? BM / 4 : BM / 2;  // A rows this CTA loads
-      const int a_row = ti.row0 + ti.m_blk * BM + static_cast<int>(rank) * a_rows;
-      const uint32_t stage_tx = 2u * (static_cast<uint32_t>(a_rows) * 128u + kPairStageB);
+      const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
+      const void* mB;
+      int b_row;
+      if (MODE == kSwiGLU) {
+        // CTA 0 holds the W_gate half of B, CTA 1 the W_up half
+        mB = leader ? (dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0))
+                    : (dense ? static_cast<const void*>(&mapB1u) : static_cast<const void*>(&mapB0u));
+        b_row = ti.b_row0 + ti.n_blk * BN;
+      } else {
+        mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
+        b_row = ti.b_row0 + ti.n_blk * BN + static_cast<int>(rank) * 128;
+      }
+      const int a_row = ti.row0 + ti.m_blk * BM + static_cast<int>(rank) * 128;
       int g4[4] = {0, 0, 0, 0};
       if (gather) {
 #pragma unroll
@@ -775,14 +764,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* sA = smem + stage * kPairStageBytes;
         uint8_t* sB = sA + kPairStageA;
         const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[stage]), 0);
-        if (lane == 0 && leader) mbar_arrive_expect_tx(&full_bar[stage], stage_tx);
+        if (lane == 0 && leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
         __syncwarp();
-        if (gather && lane * 4 < a_rows)
+        if (gather)
           tma_gather4_pair(sA + lane * 512, mA, full_leader, kb * BK, g4[0], g4[1], g4[2], g4[3]);
         if (lane == 0) {
           if (!gather) tma_load_2d_pair(sA, mA, full_leader, kb * BK, a_row);
           tma_load_2d_pair(sB, mB, full_leader, kb * BK, b_row);
-          if (MODE == kSwiGLU) tma_load_2d_pair(sB + kPairStageB / 2, mBu, full_leader, kb * BK, b_row);
         }
         if (++stage == kPairStages) {
           stage = 0;
@@ -811,7 +799,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * kAccCols;
-        const uint32_t idesc = ti.rows - ti.m_blk * BM <= BM / 2 ? idesc_half : idesc_full;
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait_bounded_cluster(&full_bar[stage], phase, abort_v, p.status, p.budget_ns,
                                          MOE_ERR_TIMEOUT)) {
@@ -861,13 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(acc) * kAccCols;
-      const bool half = ti.rows - ti.m_blk * BM <= BM / 2;
-      // half tile: lane quadrants 0,1 hold rows 0..63 for the first B half,
-      // quadrants 2,3 the same rows for the second B half
-      const int nh = quad >> 1;
-      const int row = ti.m_blk * BM +
-                      (half ? static_cast<int>(rank) * 64 + (quad & 1) * 32 + lane
-                            : static_cast<int>(rank) * 128 + row_in_tile);
+      const int row = ti.m_blk * BM + static_cast<int>(rank) * 128 + row_in_tile;
       const bool row_ok = row < ti.rows;
       const int col0 = ti.n_blk * BN;
       const int cols_left = ti.ncols - col0;
@@ -882,16 +863,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       out += col0;
       if (MODE == kSwiGLU) {
-        // each 64-column block of TMEM: 32+32 gate columns then the matching up columns
-        const int n_it = half ? 2 : 4;
 #pragma unroll 1
-        for (int it = 0; it < n_it; ++it) {
-          const int cb = (it >> 1) * 128 + (it & 1) * 32;
-          const int oc = half ? nh * 64 + it * 32 : it * 32;
+        for (int c = 0; c < 128; c += 32) {
           uint32_t gr[32], ur[32];
-          tmem_ld32_sync(tbase + cb, gr);
-          tmem_ld32_sync(tbase + cb + 64, ur);
-          if (row_ok && oc < cols_left) {
+          tmem_ld32_sync(tbase + c, gr);
+          tmem_ld32_sync(tbase + 128 + c, ur);
+          if (row_ok && c < cols_left) {
             float act[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -899,21 +876,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float uv = __uint_as_float(ur[i]);
               act[i] = gv / (1.0f + __expf(-gv)) * uv;
             }
-            store32(out + oc, act, cols_left - oc);
+            store32(out + c, act, cols_left - c);
           }
         }
       } else {
-        const int n_cols = half ? 128 : 256;
-        const int oc0 = half ? nh * 128 : 0;
 #pragma unroll 1
-        for (int c = 0; c < n_cols; c += 32) {
+        for (int c = 0; c < 256; c += 32) {
           uint32_t v[32];
           tmem_ld32_sync(tbase + c, v);
-          if (row_ok && oc0 + c < cols_left) {
+          if (row_ok && c < cols_left) {
             float f[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]) * scale;
-            store32(out + oc0 + c, f, cols_left - oc0 - c);
+            store32(out + c, f, cols_left - c);
           }
         }
       }
@@ -1036,8 +1011,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap* maps, const GemmParams& p, int p
   if (clusters > pair_tiles) clusters = pair_tiles;
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  err = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                           maps[6], maps[7], p);
+  err = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -1063,38 +1037,24 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   const int64_t R = a.rows > 0 ? a.rows : a.T * a.k;
   const bool sh = a.F_sh > 0;
   const int sms = num_sms();
-  // maps 0..5: A routed, B routed (gate / down), B routed (up), A dense, B
-  // dense, B dense (up); 6, 7: A routed / dense with the 64-row box of the
-  // pair kernel's half tiles
-  CUtensorMap m[8];
+  CUtensorMap m[6];
 
-  // CTA pairs (256-row tiles, 128-row half tiles for group tails) pay off once
-  // the experts hold enough rows on average; below that the 1-CTA kernel's
-  // 128-row tiles keep more SMs busy.
-  const bool pair = a.dtype == MOE_BF16 && R >= static_cast<int64_t>(kPairMinRowsPerExpert) * a.N;
   // pass A: act = SiLU(x Wg^T) * (x Wu^T); x is the dispatched copy, or the
   // rows of h picked by index (gather4, 1-row box) when gather_rows is given
   const bool gather = a.gather_rows != nullptr;
-  // a CTA pair holds 64 W_gate rows over 64 W_up rows per CTA
-  const uint32_t gu_box = pair ? 64 : 128;
   if (gather) {
     if (!make_map(&m[0], a.h, a.dtype, a.d, a.T, 1)) return cudaErrorInvalidValue;
-    m[6] = m[0];
-  } else {
-    if (!make_map(&m[0], a.x_disp, a.dtype, a.d, R, kBM)) return cudaErrorInvalidValue;
-    if (pair && !make_map(&m[6], a.x_disp, a.dtype, a.d, R, kBM / 2)) return cudaErrorInvalidValue;
+  } else if (!make_map(&m[0], a.x_disp, a.dtype, a.d, R, kBM)) {
+    return cudaErrorInvalidValue;
   }
-  if (!make_map(&m[1], a.W_gate, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, gu_box))
-    return cudaErrorInvalidValue;
-  if (!make_map(&m[2], a.W_up, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, gu_box))
-    return cudaErrorInvalidValue;
+  if (!make_map(&m[1], a.W_gate, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&m[2], a.W_up, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, 128)) return cudaErrorInvalidValue;
   if (sh) {
     if (!make_map(&m[3], a.h, a.dtype, a.d, a.T, kBM)) return cudaErrorInvalidValue;
-    if (pair && !make_map(&m[7], a.h, a.dtype, a.d, a.T, kBM / 2)) return cudaErrorInvalidValue;
-    if (!make_map(&m[4], a.Ws_gate, a.dtype, a.d, a.F_sh, gu_box)) return cudaErrorInvalidValue;
-    if (!make_map(&m[5], a.Ws_up, a.dtype, a.d, a.F_sh, gu_box)) return cudaErrorInvalidValue;
+    if (!make_map(&m[4], a.Ws_gate, a.dtype, a.d, a.F_sh, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&m[5], a.Ws_up, a.dtype, a.d, a.F_sh, 128)) return cudaErrorInvalidValue;
   } else {
-    m[3] = m[0]; m[4] = m[1]; m[5] = m[2]; m[7] = m[6];
+    m[3] = m[0]; m[4] = m[1]; m[5] = m[2];
   }
   GemmParams pa{};
   pa.offsets = a.offsets;
@@ -1110,6 +1070,9 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   pa.status = a.status;
   pa.budget_ns = kWaitBudgetNs;
   pa.gather_rows = a.gather_rows;
+  // CTA pairs (256-row tiles) pay off when experts hold many rows on average;
+  // with few rows per expert the 128-row tiles waste less of the MMA.
+  const bool pair = a.dtype == MOE_BF16 && R >= static_cast<int64_t>(kPairMinRowsPerExpert) * a.N;
   cudaError_t err;
   if (pair) {
     err = launch_gemm_pair<kSwiGLU>(m, pa, tiles_bound(R, a.N, a.F, 128, sh ? a.T : 0, a.F_sh, 256),
@@ -1124,7 +1087,6 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
 
   // pass B: y = act Wd^T
   if (!make_map(&m[0], a.act, a.dtype, a.F, R, kBM)) return cudaErrorInvalidValue;
-  if (pair && !make_map(&m[6], a.act, a.dtype, a.F, R, kBM / 2)) return cudaErrorInvalidValue;
   // a CTA pair splits the 256 B rows of a down tile 128/128 between its CTAs
   const uint32_t down_box = pair ? 128 : 256;
   if (!make_map(&m[1], a.W_down, a.dtype, a.F, static_cast<uint64_t>(a.N) * a.d, down_box))
@@ -1132,11 +1094,10 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   m[2] = m[1];
   if (sh) {
     if (!make_map(&m[3], a.act_sh, a.dtype, a.F_sh, a.T, kBM)) return cudaErrorInvalidValue;
-    if (pair && !make_map(&m[7], a.act_sh, a.dtype, a.F_sh, a.T, kBM / 2)) return cudaErrorInvalidValue;
     if (!make_map(&m[4], a.Ws_down, a.dtype, a.F_sh, a.d, down_box)) return cudaErrorInvalidValue;
     m[5] = m[4];
   } else {
-    m[3] = m[0]; m[4] = m[1]; m[5] = m[1]; m[7] = m[6];
+    m[3] = m[0]; m[4] = m[1]; m[5] = m[1];
   }
   GemmParams pb = pa;
   pb.gather_rows = nullptr;
