@@ -110,36 +110,58 @@ def traffic_from_profile(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples taken while the timed region runs."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """nvidia-smi clock / power / throttle samples taken while the timed region
+    runs, plus the driver's cumulative throttle-time counters read before and
+    after it."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.active")
+    # bits of clocks_event_reasons.active (NVML clocks-event reason mask)
+    BITS = ((0x1, "gpu_idle"), (0x2, "applications_clocks_setting"), (0x4, "sw_power_cap"),
+            (0x8, "hw_slowdown"), (0x10, "sync_boost"), (0x20, "sw_thermal_slowdown"),
+            (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"),
+            (0x100, "display_clock_setting"))
+    COUNTERS = ("sw_power_cap", "sw_thermal_slowdown", "hw_thermal_slowdown",
+                "hw_power_brake_slowdown", "sync_boost")
 
-    def __init__(self, gpu_index: int, interval_ms: int = 20):
+    def __init__(self, gpu_index: int, interval_ms: int = 10):
         self.gpu = gpu_index
         self.interval_ms = interval_ms
         self.proc = None
         self.lines = []
         self._t = None
+        self.c0 = self.c1 = None
+        self.t0 = self.t1 = None
+
+    def _counters(self):
+        q = ",".join(f"clocks_event_reasons_counters.{c}" for c in self.COUNTERS)
+        try:
+            r = subprocess.run(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                "-i", str(self.gpu)], capture_output=True, text=True, timeout=10)
+            vals = [float(v) for v in r.stdout.strip().split(",")]
+            return dict(zip(self.COUNTERS, vals)) if len(vals) == len(self.COUNTERS) else None
+        except (OSError, ValueError, subprocess.TimeoutExpired):
+            return None
 
     def __enter__(self):
+        self.c0 = self._counters()
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-i", str(self.gpu), "-lms", str(self.interval_ms)],
+                ["stdbuf", "-oL", "nvidia-smi", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-i", str(self.gpu), "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
             time.sleep(0.3)
         except (OSError, ValueError):
             self.proc = None
+        self.t0 = time.time()
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *a):
+        self.t1 = time.time()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -148,16 +170,17 @@ class ClockSampler:
                 self.proc.kill()
             if self._t is not None:
                 self._t.join(timeout=2)
+        self.c1 = self._counters()
 
     def summary(self):
         rows = []
-        for ln in self.lines:
+        for t, ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 5 or not (self.t0 <= t <= self.t1):
                 continue
             try:
                 rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
-                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                                 mask=int(parts[4], 16)))
             except ValueError:
                 continue
         if not rows:
@@ -166,13 +189,19 @@ class ClockSampler:
         loaded = [r for r in rows if r["power"] > 300] or rows
         reasons = set()
         for r in loaded:
-            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
-                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
-                if r[key].lower().startswith("active"):
+            for bit, name in self.BITS:
+                if r["mask"] & bit and bit != 0x1:
                     reasons.add(name)
-        return {"sm_mhz": float(np.median([r["sm"] for r in loaded])),
-                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
-                "samples": len(loaded), "power_w_max": max(r["power"] for r in rows)}
+        out = {"sm_mhz": float(np.median([r["sm"] for r in loaded])),
+               "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+               "samples": len(loaded), "samples_total": len(rows),
+               "power_w_max": max(r["power"] for r in rows),
+               "power_w_median_loaded": float(np.median([r["power"] for r in loaded]))}
+        if self.c0 is not None and self.c1 is not None:
+            # microseconds the driver spent in each throttle reason during the region
+            out["throttle_us"] = {k: round(self.c1[k] - self.c0[k]) for k in self.COUNTERS}
+            out["region_s"] = round(self.t1 - self.t0, 3)
+        return out
 
 
 # --------------------------------------------------------- CPU baseline ---
