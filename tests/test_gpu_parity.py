@@ -6,7 +6,8 @@ import pytest
 import torch
 
 from conftest import load_golden
-from gpu_helpers import (BF16_TOL, F32_TOL, assert_close_tol, assert_layer_close, check_combine,
+from gpu_helpers import (BF16_TOL, F32_TOL, assert_close_tol, assert_expert_rows_close,
+                         assert_layer_close, check_combine, expert_rows_magnitude,
                          check_selection,
                          e2e_selection_check, gpu_inputs, logit_bound, np_f, np_i, oracle_gates_from_logits,
                          out_tol, run_forward, run_staged, selection_scores)
@@ -36,6 +37,11 @@ SMALL = {
     # more experts than tokens can cover: many empty groups, N > 256
     "many_experts": Workload("many_experts", T=200, d=64, N=300, F=64, k=8, score="sigmoid",
                              bias_zipf_s=1.1),
+    # the largest expert count and top-k the ABI accepts (1024, 16): most
+    # experts idle or nearly so, 16 slots per token, shared expert, N > 256
+    # (warp-per-token router)
+    "max_experts_topk": Workload("max_experts_topk", T=300, d=64, N=1024, F=64, k=16, F_sh=64,
+                                 score="sigmoid", wr_std=0.1),
     "softmax_bias_none": Workload("softmax_bias_none", T=333, d=128, N=32, F=128, k=3,
                                   norm="none", bias_zipf_s=1.1, bias_beta=0.05),
     # >= 768 rows per expert: the grouped GEMM runs on CTA pairs (256-row tiles)
@@ -112,11 +118,22 @@ def test_small_workload_stagewise_parity(cuda_lib, name):
     assert torch.equal(r["x_disp"].cpu(), inp["h"][torch.from_numpy(row_token)])
 
     # ---- expert rows and shared expert ----
-    y_ref = O.expert_rows(o["h"][row_token], offsets, o["W_gate"], o["W_up"], o["W_down"])
-    assert_close_tol(np_f(r["y_rows"]), y_ref, out_tol(w), f"{name} y_rows")
+    x_rows = o["h"][row_token]
+    y_ref = O.expert_rows(x_rows, offsets, o["W_gate"], o["W_up"], o["W_down"])
+    if w.dtype == "f32":
+        assert_close_tol(np_f(r["y_rows"]), y_ref, out_tol(w), f"{name} y_rows")
+    else:
+        mag = expert_rows_magnitude(x_rows, offsets, o["W_gate"], o["W_up"], o["W_down"])
+        assert_expert_rows_close(np_f(r["y_rows"]), y_ref, mag, out_tol(w), f"{name} y_rows")
     if w.F_sh > 0:
         ysh_ref = O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"])
-        assert_close_tol(np_f(r["y_sh"]), ysh_ref, out_tol(w), f"{name} y_shared")
+        if w.dtype == "f32":
+            assert_close_tol(np_f(r["y_sh"]), ysh_ref, out_tol(w), f"{name} y_shared")
+        else:
+            mag_sh = expert_rows_magnitude(o["h"], np.array([0, w.T]), o["Ws_gate"][None],
+                                           o["Ws_up"][None], o["Ws_down"][None])
+            assert_expert_rows_close(np_f(r["y_sh"]), ysh_ref, mag_sh, out_tol(w),
+                                     f"{name} y_shared")
 
     # ---- combine: one rounding of the GPU's own terms ----
     check_combine(r, cfg, f"{name} combine")
@@ -127,7 +144,8 @@ def test_small_workload_stagewise_parity(cuda_lib, name):
 
 
 @pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "tiny_fp32",
-                                  "many_experts", "pair_shared_ragged_n", "pair_half_tails"])
+                                  "many_experts", "pair_shared_ragged_n", "pair_half_tails",
+                                  "max_experts_topk"])
 def test_forward_equals_stages_and_is_deterministic(cuda_lib, name):
     w = SMALL[name]
     cfg = api.config_for(w)
