@@ -34,9 +34,22 @@ from top_routing_grouped_bias_b300 import api, synth  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s; grouped-GEMM TFLOP/s & HBM GB/s vs B300 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-# route 1, dispatch 4, grouped GEMM 2, combine 1 (top-1 without a shared
-# expert: the combine happens in the down pass)
-KERNELS_PER_FORWARD = 8
+def kernels_per_forward(w) -> int:
+    """Launches of one moe_forward: route 1 (one GEMM with the top-k in its
+    epilogue, or the CUDA-core kernel) or 2 (split logits GEMM + selection,
+    when the batch has too few 128-token tiles to fill the GPU), dispatch 4,
+    grouped GEMM 2, combine 1 (top-1 without a shared expert: the combine
+    happens in the down pass)."""
+    route = 1
+    if w.dtype == "bf16" and w.N <= 256:
+        tiles = (w.T + 127) // 128
+        kb_total = (w.d + 63) // 64
+        s = max(1, min(148 // tiles if tiles else 1, max(1, kb_total // 4)))
+        kb_per = (kb_total + s - 1) // s
+        if (kb_total + kb_per - 1) // kb_per > 1:
+            route = 2
+    combine = 0 if (w.k == 1 and w.F_sh == 0) else 1
+    return route + 4 + 2 + combine
 
 
 # ------------------------------------------------------------ host logic ---
@@ -410,8 +423,7 @@ def bench_ours(args, w):
         "stages_ms": {"route": round(route_ms, 4), "dispatch": round(disp_ms, 4),
                       "grouped_gemm": round(ffn_ms, 4), "combine": round(comb_ms, 4)},
         "next_rows": next_rows,
-        "gpu_launches": (KERNELS_PER_FORWARD - (1 if w.k == 1 and w.F_sh == 0 else 0))
-                        * args.steps,
+        "gpu_launches": kernels_per_forward(w) * args.steps,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_host.numel() * h_host.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},

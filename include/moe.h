@@ -96,10 +96,16 @@ size_t moe_workspace_size(const moe_config* cfg);
  *   idx        [T, k] int32 out: selected experts, by descending selection
  *              score; equal scores go to the lower expert index first
  *   gate       [T, k] fp32 out: gate weight of each selected expert
- *   ws         optional (may be NULL): when given, device-side failures are
- *              recorded in its status word
- * bf16 routing from h with N <= 256 runs on the tensor cores (fp32
- * accumulation); fp32 inputs, N > 256 and routing from logits run on CUDA cores.
+ *   ws         workspace of moe_workspace_size(cfg) bytes, 256-byte aligned.
+ *              Required for bf16 routing from h with N <= 256 (it holds the
+ *              tensor-core GEMM's partial logits; MOE_ERR_WORKSPACE without
+ *              it); optional otherwise. When given, device-side failures are
+ *              recorded in its status word.
+ * bf16 routing from h with N <= 256 computes the logits on the tensor cores
+ * (fp32 accumulation; a small batch splits the sum over d into slices that are
+ * added in a fixed order); fp32 inputs, N > 256 and routing from logits
+ * compute them on CUDA cores. Scores, bias, top-k and gates then run in one
+ * warp-per-token kernel for every source of logits.
  */
 moe_status moe_route(const moe_config* cfg, const void* h, const void* W_r,
                      const float* b_r, const float* sel_bias,
@@ -239,9 +245,9 @@ typedef struct {
 /* moe_route with group-limited selection; arguments as moe_route plus `grp`.
  * Scores, bias and gates are as in moe_route (gates from the un-biased scores
  * of the selected experts). Invalid group settings, including fewer than k
- * candidates in the kept groups, return MOE_ERR_INVALID_ARG. Routing from h
- * needs the workspace (moe_workspace_size) for the logits when logits_out is
- * NULL. */
+ * candidates in the kept groups, return MOE_ERR_INVALID_ARG. bf16 routing
+ * from h with N <= 256 needs the workspace (moe_workspace_size) for the
+ * tensor-core GEMM's partial logits, as moe_route does. */
 moe_status moe_route_grouped(const moe_config* cfg, const moe_group_config* grp, const void* h,
                              const void* W_r, const float* b_r, const float* sel_bias,
                              const float* logits_in, float* logits_out, int32_t* idx,

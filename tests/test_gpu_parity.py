@@ -37,6 +37,10 @@ SMALL = {
     # more experts than tokens can cover: many empty groups, N > 256
     "many_experts": Workload("many_experts", T=200, d=64, N=300, F=64, k=8, score="sigmoid",
                              bias_zipf_s=1.1),
+    # few tokens, wide d: the router's logits GEMM splits d into 4 slices
+    # whose partial logits the selection adds in order; sigmoid + bias, k=6
+    "split_router": Workload("split_router", T=40, d=1024, N=64, F=64, k=6, score="sigmoid",
+                             bias_zipf_s=1.1, bias_beta=0.3),
     # the largest expert count and top-k the ABI accepts (1024, 16): most
     # experts idle or nearly so, 16 slots per token, shared expert, N > 256
     # (warp-per-token router)

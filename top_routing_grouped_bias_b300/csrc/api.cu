@@ -45,7 +45,8 @@ P* at(void* ws, size_t off) {
 
 moe_status route_impl(const moe_config* cfg, const void* h, const void* W_r, const float* b_r,
                       const float* sel_bias, const float* logits_in, float* logits_out,
-                      int32_t* idx, float* gate, int32_t* status, cudaStream_t stream) {
+                      int32_t* idx, float* gate, int32_t* status, float* partials,
+                      cudaStream_t stream) {
   if (h != nullptr) {
     if (!ok_tensor(h) || !ok_tensor(W_r)) return MOE_ERR_INVALID_ARG;
   } else if (!ok_f32(logits_in)) {
@@ -60,7 +61,16 @@ moe_status route_impl(const moe_config* cfg, const void* h, const void* W_r, con
   a.logits_out = logits_out; a.idx = idx; a.gate = gate; a.T = cfg->T; a.d = cfg->d;
   a.N = cfg->N; a.k = cfg->k; a.score = cfg->score; a.norm = cfg->norm; a.dtype = cfg->dtype;
   a.status = status;
+  a.partials = partials;
+  if (route_on_tensor_cores(a) && partials == nullptr) return MOE_ERR_WORKSPACE;
   return from_cuda(launch_route(a, stream));
+}
+
+// The router's partial-logit scratch when the workspace holds it, else null.
+float* route_scratch(const moe_config* cfg, void* ws, size_t ws_bytes) {
+  const WsLayout L = ws_layout(*cfg);
+  if (ws == nullptr || ws_bytes < L.end_route || !aligned(ws, 256)) return nullptr;
+  return at<float>(ws, L.route_part);
 }
 
 moe_status dispatch_impl(const moe_config* cfg, const void* h, const int32_t* idx, int32_t* counts,
@@ -137,11 +147,12 @@ moe_status moe_route(const moe_config* cfg, const void* h, const void* W_r, cons
                      int32_t* idx, float* gate, void* ws, size_t ws_bytes, cudaStream_t stream) {
   moe_status s = check_config(cfg);
   if (s != MOE_OK) return s;
-  // the workspace is optional here; when given, its status word records
-  // device-side failures of the router's bounded waits
+  // the status word records device-side failures of the router's bounded
+  // waits; the tensor-core router also keeps its partial logits there
   int32_t* status = (ws != nullptr && ws_bytes >= 256 && aligned(ws, 256))
                         ? static_cast<int32_t*>(ws) : nullptr;
-  return route_impl(cfg, h, W_r, b_r, sel_bias, logits_in, logits_out, idx, gate, status, stream);
+  return route_impl(cfg, h, W_r, b_r, sel_bias, logits_in, logits_out, idx, gate, status,
+                    route_scratch(cfg, ws, ws_bytes), stream);
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const void* h, const int32_t* idx, int32_t* counts,
@@ -217,7 +228,7 @@ moe_status forward_impl(const moe_config* cfg, int64_t capacity, const void* h, 
   void* y_sh = cfg->ffn_shared > 0 ? at<void>(ws, L.y_sh) : nullptr;
 
   s = route_impl(cfg, h, W_r, b_r, sel_bias, nullptr, logits_out, idx, gate,
-                 at<int32_t>(ws, L.status), stream);
+                 at<int32_t>(ws, L.status), at<float>(ws, L.route_part), stream);
   if (s != MOE_OK) return s;
   // The dispatched copy feeds the gate/up pass with one 16 KB TMA box per
   // stage; reading the rows from h by index (gather4, moe_expert_ffn_gather)
@@ -274,25 +285,10 @@ moe_status moe_route_grouped(const moe_config* cfg, const moe_group_config* grp,
   int32_t* status = (ws != nullptr && ws_bytes >= 256 && aligned(ws, 256))
                         ? static_cast<int32_t*>(ws) : nullptr;
   a.status = status;
-  if (h != nullptr && cfg->dtype == MOE_BF16 && N <= 256 && a.n_group > 1) {
-    // logits on the tensor cores, then the grouped selection from them
-    float* z = logits_out;
-    if (z == nullptr) {
-      const WsLayout L = ws_layout(*cfg);
-      if (!ws_ok(ws, ws_bytes, L.total)) return MOE_ERR_WORKSPACE;
-      z = at<float>(ws, L.logits);
-    }
-    RouteArgs t = a;
-    t.n_group = 1;
-    t.logits_out = z;
-    s = from_cuda(launch_route(t, stream));
-    if (s != MOE_OK) return s;
-    a.h = nullptr;
-    a.W_r = nullptr;
-    a.b_r = nullptr;  // already inside z
-    a.logits_in = z;
-    a.logits_out = nullptr;
-  }
+  // bf16 from h: logits on the tensor cores, then the group pass and the
+  // selection in the warp-per-token kernel from the partial logits
+  a.partials = route_scratch(cfg, ws, ws_bytes);
+  if (route_on_tensor_cores(a) && a.partials == nullptr) return MOE_ERR_WORKSPACE;
   return from_cuda(launch_route(a, stream));
 }
 
@@ -365,7 +361,8 @@ moe_status moe_forward_expert_choice(const moe_config* cfg, int64_t capacity, co
   float* z = logits_out != nullptr ? logits_out : at<float>(ws, L.logits);
   // logits through the router (its top-k output goes to scratch)
   s = route_impl(cfg, h, W_r, b_r, nullptr, nullptr, z, at<int32_t>(ws, L.row_token),
-                 at<float>(ws, L.inv), at<int32_t>(ws, L.status), stream);
+                 at<float>(ws, L.inv), at<int32_t>(ws, L.status), at<float>(ws, L.route_part),
+                 stream);
   if (s != MOE_OK) return s;
   EcArgs e{};
   e.logits = z;

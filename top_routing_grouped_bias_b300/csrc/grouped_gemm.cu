@@ -22,10 +22,17 @@
 // W_up, so one N=256 MMA produces the gate half (columns 0..127) and the up
 // half (128..255) of a 128-column output tile.
 //
-// A third instance (kRoute) is the router: logits = h W_r^T for 128 tokens per
-// tile with all N <= 256 experts in one accumulator; its epilogue gives each
-// thread one token's logit row straight from TMEM and does softmax / sigmoid,
-// the selection bias, the top-k with the lowest-index tie-break and the gates.
+// Two more instances are the router: logits = h W_r^T for 128 tokens per tile
+// with all N <= 256 experts in one accumulator.
+//   kRoute   (batches of at least ~148 token tiles) does the whole routing in
+//            its epilogue: each thread takes one token's logit row from TMEM
+//            and computes softmax / sigmoid, the selection bias, the top-k
+//            with the lowest-index tie-break and the gates, overlapped with
+//            the next tile's MMAs.
+//   kLogits  (smaller batches) splits the reduction over d into slices (one
+//            work unit per tile and slice) so that enough SMs stream h; each
+//            unit writes its fp32 partial logits and the warp-per-token
+//            selection kernel (route.cu) adds the slices in slice order.
 //
 // Tiles of one group are ordered in bands of at most 16 m-tiles: inside a band
 // the n-tiles advance slowest, so CTAs running side by side share one weight
@@ -69,7 +76,7 @@ constexpr uint64_t kWaitBudgetNs = 4000000000ull;   // 4 s per wait
 constexpr int kPairMinRowsPerExpert = MOE_PAIR_MIN_ROWS;
 constexpr uint64_t kDrainBudgetNs = 200000000ull;   // 0.2 s
 
-enum { kSwiGLU = 0, kDown = 1, kRoute = 2 };
+enum { kSwiGLU = 0, kDown = 1, kRoute = 2, kLogits = 3 };
 
 // Router epilogue arguments (kRoute only).
 struct RouteEpi {
@@ -95,6 +102,11 @@ struct GemmParams {
   int32_t* status;
   uint64_t budget_ns;
   RouteEpi re;
+  // kLogits: fp32 partial logits [k_splits][rows_routed][n_out]; work unit u
+  // is token tile u / k_splits and reduction slice u % k_splits of
+  // kb_per_split 64-element blocks
+  float* partials;
+  int32_t k_splits, kb_per_split;
   // Down pass with top-1 routing and no shared expert: the combine is a
   // scaled scatter, so the epilogue writes gate * y to the token's output row
   // (out = [T, n_out]) instead of writing y_rows. Null: plain y_rows.
@@ -143,6 +155,24 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int* tile_start,
   const int bs = min(band_sz, mt - band * band_sz);
   ti.n_blk = r / bs;
   ti.m_blk = band * band_sz + (r - ti.n_blk * bs);
+  return ti;
+}
+
+// kLogits work unit: token tile and reduction slice; kb0 = first K block.
+__device__ __forceinline__ TileInfo logits_tile(int unit, const GemmParams& p, int& split,
+                                                int& kb0) {
+  TileInfo ti;
+  split = unit % p.k_splits;
+  ti.g = 0;
+  ti.m_blk = unit / p.k_splits;
+  ti.n_blk = 0;
+  ti.row0 = 0;
+  ti.rows = p.rows_routed;
+  ti.ncols = p.n_out;
+  ti.b_row0 = 0;
+  kb0 = split * p.kb_per_split;
+  const int kb_total = (p.K + 63) / 64;
+  ti.num_kb = min(p.kb_per_split, kb_total - kb0);
   return ti;
 }
 
@@ -336,10 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mapB1u, const GemmParams p) {
   constexpr int BK = 128 / static_cast<int>(sizeof(T));   // elements per 128-byte row
   constexpr int BN = MODE == kSwiGLU ? 128 : 256;         // output columns per tile
-  // kRoute: one accumulator of n_out = N rounded up to 16 columns
-  const int mma_n = MODE == kRoute ? p.n_out : 256;
+  // kRoute / kLogits: one accumulator of n_out = N rounded up to 16 columns
+  constexpr bool kRouter = MODE == kRoute || MODE == kLogits;
+  const int mma_n = kRouter ? p.n_out : 256;
   const uint32_t idesc = make_idesc(kBM, mma_n, sizeof(T) == 2 ? 1u : 2u);
-  const uint32_t stage_tx = MODE == kRoute ? kStageA + static_cast<uint32_t>(mma_n) * 128u : kStageBytes;
+  const uint32_t stage_tx = kRouter ? kStageA + static_cast<uint32_t>(mma_n) * 128u : kStageBytes;
 
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -381,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&mapB0);
       if (MODE == kSwiGLU) tma_prefetch_desc(&mapB0u);
     }
-    if (MODE == kRoute) {
+    if (kRouter) {
       if (lane == 0) { grp_off[0] = 0; grp_off[1] = p.rows_routed; }
     } else {
       for (int g = lane; g <= p.n_routed; g += 32) grp_off[g] = p.offsets[g];
@@ -403,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (g < G) {
         const int rows = g < p.n_routed ? grp_off[g + 1] - grp_off[g] : p.rows_shared;
         const int ncols = g < p.n_routed ? p.n_out : p.n_out_shared;
-        tiles = ((rows + kBM - 1) / kBM) * ((ncols + BN - 1) / BN);
+        tiles = ((rows + kBM - 1) / kBM) * (MODE == kLogits ? p.k_splits : (ncols + BN - 1) / BN);
       }
       int incl = tiles;
 #pragma unroll
@@ -431,7 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0, issued_mask = 0, issued_par = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const TileInfo ti = decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+      int split = 0, kb0 = 0;
+      const TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
+                                          : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
       const bool dense = ti.g >= p.n_routed;
       const bool gather = MODE == kSwiGLU && p.gather_rows != nullptr && !dense;
       const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
@@ -462,14 +495,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* sA = smem + stage * kStageBytes;
         uint8_t* sB = sA + kStageA;
-        if (gather) tma_gather4(sA + lane * 512, mA, &full_bar[stage], kb * BK, g4[0], g4[1], g4[2], g4[3]);
+        if (gather) tma_gather4(sA + lane * 512, mA, &full_bar[stage], (kb0 + kb) * BK, g4[0], g4[1], g4[2], g4[3]);
         if (lane == 0) {
-          if (!gather) tma_load_2d(sA, mA, &full_bar[stage], kb * BK, a_row);
+          if (!gather) tma_load_2d(sA, mA, &full_bar[stage], (kb0 + kb) * BK, a_row);
           if (MODE == kSwiGLU) {
-            tma_load_2d(sB, mB, &full_bar[stage], kb * BK, b_row);
-            tma_load_2d(sB + kStageB / 2, mBu, &full_bar[stage], kb * BK, b_row);
+            tma_load_2d(sB, mB, &full_bar[stage], (kb0 + kb) * BK, b_row);
+            tma_load_2d(sB + kStageB / 2, mBu, &full_bar[stage], (kb0 + kb) * BK, b_row);
           } else {
-            tma_load_2d(sB, mB, &full_bar[stage], kb * BK, b_row);
+            tma_load_2d(sB, mB, &full_bar[stage], (kb0 + kb) * BK, b_row);
           }
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -491,7 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+        int split = 0, kb0 = 0;
+        const TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
+                                            : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
         if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, abort_v, p.status, p.budget_ns,
                                MOE_ERR_TIMEOUT)) {
           ok = false;
@@ -543,7 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileInfo ti = decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+      int split = 0, kb0 = 0;
+      const TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
+                                          : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_v, p.status, p.budget_ns,
                              MOE_ERR_TIMEOUT))
         break;
@@ -566,6 +603,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       out += col0;
       if (MODE == kRoute) {
         route_epilogue<KT>(tbase, row, row_ok, p.n_out, p.re);
+      } else if (MODE == kLogits) {
+        // this unit's partial logits, rows of the tile x n_out columns
+        float* dst = p.partials +
+                     (static_cast<size_t>(split) * p.rows_routed + static_cast<size_t>(row)) * p.n_out;
+#pragma unroll 1
+        for (int c = 0; c < p.n_out; c += 32) {
+          uint32_t v[32];
+          tmem_ld32_sync(tbase + c, v);
+          if (row_ok) {
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+            store32(dst + c, f, p.n_out - c);
+          }
+        }
       } else if (MODE == kSwiGLU) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
@@ -1118,7 +1170,33 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
 }
 
 bool route_on_tensor_cores(const RouteArgs& a) {
-  return a.h != nullptr && a.dtype == MOE_BF16 && a.N <= 256 && a.n_group <= 1;
+  return a.h != nullptr && a.dtype == MOE_BF16 && a.N <= 256;
+}
+
+cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t stream) {
+  const RouteSplit rs = route_split(a.T, a.d, a.N);
+  CUtensorMap m[6];
+  if (!make_map(&m[0], a.h, a.dtype, a.d, a.T, kBM)) return cudaErrorInvalidValue;
+  if (!make_map(&m[1], a.W_r, a.dtype, a.d, a.N, static_cast<uint32_t>(rs.n_pad)))
+    return cudaErrorInvalidValue;
+  m[2] = m[1]; m[3] = m[0]; m[4] = m[1]; m[5] = m[1];
+  GemmParams p{};
+  p.offsets = nullptr;
+  p.n_routed = 1;
+  p.rows_routed = static_cast<int32_t>(a.T);
+  p.rows_shared = 0;
+  p.K = a.d;
+  p.K_shared = a.d;
+  p.n_out = rs.n_pad;
+  p.n_out_shared = 0;
+  p.status = a.status;
+  p.budget_ns = kWaitBudgetNs;
+  p.partials = a.partials;
+  p.k_splits = rs.splits;
+  p.kb_per_split = rs.kb_per_split;
+  const int64_t units = (a.T + kBM - 1) / kBM * rs.splits;
+  const int grid = static_cast<int>(units < num_sms() ? units : num_sms());
+  return launch_gemm<kLogits, __nv_bfloat16>(m, p, grid, stream);
 }
 
 cudaError_t launch_route_mma(const RouteArgs& a, cudaStream_t stream) {

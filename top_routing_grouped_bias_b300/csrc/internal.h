@@ -17,13 +17,38 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline int elem_size(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 
+// The router's logits GEMM (bf16 from h, N <= 256) splits the reduction over
+// d into S slices when the batch has fewer 128-token tiles than there are
+// SMs to stream h: S = min(max(1, 148 / tiles), max(1, ceil(d / 64) / 4)),
+// each slice a whole number of (at least four) 64-element blocks, none empty. The plan depends on
+// (T, d) only, so the partial sums and their order are the same on every
+// device. Each slice writes fp32 partial logits [T, n_pad] (n_pad = N rounded
+// up to 16); the selection kernel adds the slices in slice order.
+constexpr int kRouteSplitTarget = 148;
+struct RouteSplit {
+  int splits, kb_per_split, n_pad;
+};
+inline RouteSplit route_split(int64_t T, int d, int N) {
+  RouteSplit r{};
+  const int64_t tiles = (T + 127) / 128;
+  const int kb_total = (d + 63) / 64;
+  int64_t s = tiles > 0 ? kRouteSplitTarget / tiles : 1;
+  const int64_t s_max = kb_total / 4 > 1 ? kb_total / 4 : 1;
+  if (s > s_max) s = s_max;
+  if (s < 1) s = 1;
+  r.kb_per_split = static_cast<int>((kb_total + s - 1) / s);
+  r.splits = (kb_total + r.kb_per_split - 1) / r.kb_per_split;
+  r.n_pad = (N + 15) / 16 * 16;
+  return r;
+}
+
 // Workspace layout. Every region starts on a 256-byte boundary. The entry
-// points use the prefixes they need: dispatch [status, block_base],
-// expert FFN [status .. act_sh], forward everything.
+// points use the prefixes they need: route [status, route_part], dispatch
+// [status .. block_base], expert FFN [status .. act_sh], forward everything.
 struct WsLayout {
-  size_t status, block_base, stats, act, act_sh, offsets, counts, row_token, inv, x_disp, y_rows,
-      y_sh, logits, ec_scores, ec_choice;
-  size_t end_dispatch, end_ffn, total;
+  size_t status, route_part, block_base, stats, act, act_sh, offsets, counts, row_token, inv,
+      x_disp, y_rows, y_sh, logits, ec_scores, ec_choice;
+  size_t end_route, end_dispatch, end_ffn, total;
 };
 
 inline WsLayout ws_layout(const moe_config& c) {
@@ -38,6 +63,11 @@ inline WsLayout ws_layout(const moe_config& c) {
     return at;
   };
   L.status = take(256);
+  // partial logits of the split router GEMM (bf16 from h, N <= 256)
+  const RouteSplit rs = route_split(c.T, c.d, c.N);
+  const bool tc_router = c.dtype == MOE_BF16 && c.N <= 256;
+  L.route_part = take(tc_router ? static_cast<size_t>(rs.splits) * T * rs.n_pad * 4 : 0);
+  L.end_route = o;
   L.block_base = take(nb * static_cast<size_t>(c.N) * 4);
   L.stats = take(nb * (2 * static_cast<size_t>(c.N) + 2) * 4);
   L.end_dispatch = o;
@@ -69,15 +99,23 @@ struct RouteArgs {
   int32_t* idx;
   float* gate;
   int32_t* status;  // device status word or null
+  // tensor-core router: scratch for the split partial logits [splits][T][n_pad]
+  // (route_split); the selection reads n_partials slices of row stride ld_partial
+  float* partials;
+  int32_t n_partials, ld_partial;
   int64_t T;
   int32_t d, N, k, score, norm, dtype;
   // group-limited selection (n_group <= 1: off)
   int32_t n_group, topk_group, group_rule, top_m;
 };
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
-// Router as a tcgen05 GEMM with a top-k epilogue (bf16, N <= 256, from h).
+// Router on the tensor cores (bf16, N <= 256, from h). With one slice in
+// route_split(T, d, N) a single GEMM does the routing in its epilogue
+// (launch_route_mma); otherwise the split GEMM writes the partial logits to
+// a.partials (launch_route_logits) and the selection runs in route.cu.
 bool route_on_tensor_cores(const RouteArgs& a);
 cudaError_t launch_route_mma(const RouteArgs& a, cudaStream_t stream);
+cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t stream);
 
 // ---- dispatch ----
 struct DispatchArgs {

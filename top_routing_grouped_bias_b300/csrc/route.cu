@@ -1,7 +1,9 @@
 // Router: logits, scores, top-k selection and gates, one warp per token.
-// This SIMT kernel serves fp32 inputs, N > 256 experts and routing from given
-// logits; bf16 routing from h with N <= 256 runs as a tcgen05 GEMM with the
-// same selection rules in its epilogue (grouped_gemm.cu, kRoute).
+// The logits come from one of three sources: this kernel's own dot products
+// (fp32 inputs, N > 256), logits given by the caller, or the partial logits of
+// the split tcgen05 GEMM (bf16 from h, N <= 256; grouped_gemm.cu, kLogits),
+// which are added here slice by slice in slice order. Selection and gates are
+// the same code for all three.
 //
 // Pages: "MOE 专家选择与路由机制" §二 (z = W_r h + b_r; softmax; TopK; renormalise
 // over the selected experts); "MoE：router 怎样选 expert" (softmax over the
@@ -101,6 +103,22 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
         for (int ee = 0; ee < ne; ++ee)
           z[e0 + ee] = acc[ee] + (a.b_r != nullptr ? a.b_r[e0 + ee] : 0.f);
       }
+    }
+  } else if (a.partials != nullptr) {
+    // slices added in slice order, four loads in flight
+    const size_t slice = static_cast<size_t>(a.T) * a.ld_partial;
+    const float* zp = a.partials + static_cast<size_t>(t) * a.ld_partial;
+    for (int e = lane; e < N; e += 32) {
+      float v = 0.f;
+      for (int sl = 0; sl < a.n_partials; sl += 4) {
+        float w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] = sl + u < a.n_partials ? zp[(sl + u) * slice + e] : 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (sl + u < a.n_partials) v += w[u];
+      }
+      z[e] = v + (a.b_r != nullptr ? a.b_r[e] : 0.f);
     }
   } else {
     const float* zin = a.logits_in + t * N;
@@ -244,9 +262,26 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
 
 }  // namespace
 
-cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
-  if (a.T == 0) return cudaSuccess;
-  if (route_on_tensor_cores(a)) return launch_route_mma(a, stream);
+cudaError_t launch_route(const RouteArgs& in, cudaStream_t stream) {
+  if (in.T == 0) return cudaSuccess;
+  RouteArgs a = in;
+  if (route_on_tensor_cores(in)) {
+    // one slice: the GEMM routes in its epilogue
+    if (route_split(in.T, in.d, in.N).splits == 1 && in.n_group <= 1)
+      return launch_route_mma(in, stream);
+    // split partial logits on the tensor cores, selection below from them
+    if (in.partials == nullptr) return cudaErrorInvalidValue;
+    const cudaError_t e = launch_route_logits(in, stream);
+    if (e != cudaSuccess) return e;
+    const RouteSplit rs = route_split(in.T, in.d, in.N);
+    a.h = nullptr;
+    a.W_r = nullptr;
+    a.logits_in = nullptr;
+    a.n_partials = rs.splits;
+    a.ld_partial = rs.n_pad;
+  } else {
+    a.partials = nullptr;
+  }
   const bool two = a.sel_bias != nullptr || a.n_group > 1;
   const size_t smem = static_cast<size_t>(kRouteWarps) * a.N * (two ? 2 : 1) * sizeof(float);
   const unsigned grid = static_cast<unsigned>((a.T + kRouteWarps - 1) / kRouteWarps);
