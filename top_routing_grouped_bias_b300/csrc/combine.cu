@@ -7,8 +7,10 @@
 //
 //   out[t] = y_shared[t] + sum_{j<k} gate[t,j] * y_rows[inv[t*k+j]]
 //
-// One thread per 16-byte vector of out; fp32 accumulation in slot order
-// (deterministic), rounded once to the output dtype.
+// A block takes one token at a time (blocks stride over the tokens) and reads
+// its k rows and gates once; its threads stride over the row's 16-byte
+// vectors. fp32 accumulation in slot order (deterministic), rounded once to
+// the output dtype.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -45,37 +47,51 @@ template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   constexpr int V = 16 / sizeof(T);
   const int nvec = a.d / V;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= a.T * nvec) return;
-  const int64_t t = i / nvec;
-  const int v = static_cast<int>(i - t * nvec);
   const uint4* Y = static_cast<const uint4*>(a.y_rows);
-  float acc[V];
-  if (a.y_shared != nullptr) {
-    unpack(static_cast<const uint4*>(a.y_shared)[i], acc, static_cast<T*>(nullptr));
-  } else {
+  const uint4* S = static_cast<const uint4*>(a.y_shared);
+  uint4* O = static_cast<uint4*>(a.out);
+  const int64_t R = a.T * a.k;
+  // the token's rows (first vector, -1 = none) and gates in slot order; only
+  // rows moe_dispatch wrote are read
+  __shared__ int64_t rows[kMaxTopK];
+  __shared__ float g[kMaxTopK];
+  for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+    __syncthreads();  // the previous token's rows are no longer read
+    if (threadIdx.x < a.k) {
+      const int64_t r = a.inv[t * a.k + threadIdx.x];
+      const bool ok = r >= 0 && r < R;
+      rows[threadIdx.x] = ok ? r * nvec : -1;
+      g[threadIdx.x] = ok ? a.gate[t * a.k + threadIdx.x] : 0.f;
+    }
+    __syncthreads();
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      float acc[V];
+      if (S != nullptr) {
+        unpack(S[t * nvec + v], acc, static_cast<T*>(nullptr));
+      } else {
 #pragma unroll
-    for (int q = 0; q < V; ++q) acc[q] = 0.f;
-  }
-  for (int j = 0; j < a.k; ++j) {
-    const int64_t row = a.inv[t * a.k + j];
-    if (row < 0 || row >= a.T * a.k) continue;  // only rows moe_dispatch wrote are read
-    const float g = a.gate[t * a.k + j];
-    float y[V];
-    unpack(Y[row * nvec + v], y, static_cast<T*>(nullptr));
+        for (int q = 0; q < V; ++q) acc[q] = 0.f;
+      }
+#pragma unroll 4
+      for (int j = 0; j < a.k; ++j) {
+        if (rows[j] >= 0) {
+          float y[V];
+          unpack(Y[rows[j] + v], y, static_cast<T*>(nullptr));
 #pragma unroll
-    for (int q = 0; q < V; ++q) acc[q] = fmaf(g, y[q], acc[q]);
+          for (int q = 0; q < V; ++q) acc[q] = fmaf(g[j], y[q], acc[q]);
+        }
+      }
+      O[t * nvec + v] = pack(acc, static_cast<T*>(nullptr));
+    }
   }
-  static_cast<uint4*>(a.out)[i] = pack(acc, static_cast<T*>(nullptr));
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
-  const int V = a.dtype == MOE_F32 ? 4 : 8;
-  const int64_t total = a.T * (a.d / V);
-  const unsigned grid = static_cast<unsigned>((total + 255) / 256);
+  const int64_t blocks = static_cast<int64_t>(num_sms()) * 8;
+  const unsigned grid = static_cast<unsigned>(a.T < blocks ? a.T : blocks);
   if (a.dtype == MOE_F32)
     combine_kernel<float><<<grid, 256, 0, stream>>>(a);
   else

@@ -3,16 +3,19 @@
 // Pages: "MOE 专家选择与路由机制" §三 Token Dispatch (pairs of one expert are
 // listed together, tokens ascending); "【大模型】MoE（专家混合模型）简介" §3 ②.
 //
-// Deterministic counting sort in three launches, no atomics on the ordering:
-//   1. count    per block of 256 tokens, per-expert pair counts -> base[b][e]
+// Deterministic counting sort in three launches plus the gather, no atomics on
+// the ordering:
+//   1. count    per block of 256 tokens, per-expert pair counts -> base[e][b]
+//               (expert-major, so that each expert's column is contiguous)
 //   2. scan     counts[e] = sum_b (capped at the capacity when one is set),
-//               offsets = exclusive scan over e, base[b][e] = sum_{b' < b} count[b'][e]
+//               offsets = exclusive scan over e, base[e][b] = sum_{b' < b} count[b'][e]
+//               (one warp per expert column, 32 blocks per warp-scan step)
 //   3. permute  per block: per-warp counts, scan over warps, then the rank of
 //               each pair among earlier pairs of the same expert in its warp;
 //               rank = base + warp prefix + in-warp rank; row = offsets[e] + rank,
 //               or inv = -1 when rank >= capacity. Writes row_token and inv.
-//   4. gather   one thread per 16-byte vector of h: reads h[t] once, writes
-//               it to the token's k dispatched rows.
+//   4. gather   a block per token at a time, a thread per 16-byte vector of
+//               the row: reads h[t] once, writes it to the token's k rows.
 // The row of (t, e) is offsets[e] + #{t' < t : e in S_t'}, i.e. rows are
 // ordered by (expert, token).
 #include <cuda_bf16.h>
@@ -40,8 +43,9 @@ __global__ void __launch_bounds__(kTB) dispatch_count_kernel(DispatchArgs a) {
     }
   }
   __syncthreads();
-  int32_t* base = a.block_base + static_cast<size_t>(blockIdx.x) * a.N;
-  for (int e = threadIdx.x; e < a.N; e += blockDim.x) base[e] = hist[e];
+  // expert-major: base[e][b] for the scan's contiguous per-expert columns
+  for (int e = threadIdx.x; e < a.N; e += blockDim.x)
+    a.block_base[static_cast<size_t>(e) * gridDim.x + blockIdx.x] = hist[e];
 }
 
 // One block of 1024 threads.
@@ -49,17 +53,35 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(DispatchArgs a, int
   __shared__ int tot[kMaxExperts];
   __shared__ int warp_sums[32];
   const int N = a.N;
-  // per-expert running sum over blocks (exclusive), column by column
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      int32_t* p = a.block_base + static_cast<size_t>(b) * N + e;
-      const int c = *p;
-      *p = run;
-      run += c;
+  // per-expert exclusive running sum over blocks: a warp takes one expert's
+  // column, 32 blocks per step (warp scan), four steps' loads in flight
+  {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int e = w; e < N; e += nw) {
+      int carry = 0;
+      for (int b0 = 0; b0 < nb; b0 += 128) {
+        int c[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int b = b0 + 32 * u + lane;
+          c[u] = b < nb ? a.block_base[static_cast<size_t>(e) * nb + b] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int b = b0 + 32 * u + lane;
+          int incl = c[u];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+          }
+          if (b < nb) a.block_base[static_cast<size_t>(e) * nb + b] = carry + incl - c[u];
+          carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+      }
+      // rows kept for this expert: all of them, or its first `capacity` pairs
+      if (lane == 0) tot[e] = a.cap_enabled && carry > a.capacity ? static_cast<int>(a.capacity) : carry;
     }
-    // rows kept for this expert: all of them, or its first `capacity` pairs
-    tot[e] = a.cap_enabled && run > a.capacity ? static_cast<int>(a.capacity) : run;
   }
   __syncthreads();
   // exclusive scan of tot[0..N) with one block: each thread owns a contiguous chunk
@@ -117,9 +139,8 @@ __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
   __syncthreads();
   // per expert: exclusive scan over warps, plus the block's rank base (the
   // number of the expert's pairs in earlier blocks)
-  const int32_t* base = a.block_base + static_cast<size_t>(blockIdx.x) * N;
   for (int e = threadIdx.x; e < N; e += blockDim.x) {
-    int run = base[e];
+    int run = a.block_base[static_cast<size_t>(e) * gridDim.x + blockIdx.x];
     for (int w = 0; w < kWarps; ++w) {
       const int c = whist[w * N + e];
       whist[w * N + e] = run;
@@ -150,21 +171,29 @@ __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
   }
 }
 
-// Gather: one thread per 16-byte vector of h; it reads h[t] once and writes
-// the vector into each of the token's k dispatched rows (coalesced along d).
+// Gather: a block takes one token at a time (blocks stride over the tokens);
+// its threads stride over the row's 16-byte vectors, read each from h once
+// and write it to the token's k dispatched rows (coalesced along d).
 template <typename T>
 __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a) {
   const int nvec = a.d * static_cast<int>(sizeof(T)) / 16;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= a.T * nvec) return;
-  const int64_t t = i / nvec;
-  const int v = static_cast<int>(i - t * nvec);
-  const uint4 val = static_cast<const uint4*>(a.h)[i];
+  const uint4* H = static_cast<const uint4*>(a.h);
   uint4* X = static_cast<uint4*>(a.x_disp);
   const int64_t R = a.T * a.k;
-  for (int j = 0; j < a.k; ++j) {
-    const int64_t row = a.inv[t * a.k + j];
-    if (row >= 0 && row < R) X[row * nvec + v] = val;
+  __shared__ int64_t rows[kMaxTopK];  // first vector of each kept row, -1 = none
+  for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+    __syncthreads();  // the previous token's rows are no longer read
+    if (threadIdx.x < a.k) {
+      const int64_t r = a.inv[t * a.k + threadIdx.x];
+      rows[threadIdx.x] = (r >= 0 && r < R) ? r * nvec : -1;
+    }
+    __syncthreads();
+    const uint4* src = H + t * nvec;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      const uint4 val = src[v];
+      for (int j = 0; j < a.k; ++j)
+        if (rows[j] >= 0) X[rows[j] + v] = val;
+    }
   }
 }
 
@@ -186,9 +215,8 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   dispatch_permute_kernel<<<nb, kTB, smem, stream>>>(a);
   if (a.x_disp != nullptr) {
-    const int vec = a.dtype == MOE_F32 ? 4 : 8;
-    const int64_t total = a.T * (a.d / vec);
-    const unsigned grid = static_cast<unsigned>((total + 255) / 256);
+    const int64_t blocks = static_cast<int64_t>(num_sms()) * 8;
+    const unsigned grid = static_cast<unsigned>(a.T < blocks ? a.T : blocks);
     if (a.dtype == MOE_F32)
       dispatch_gather_kernel<float><<<grid, 256, 0, stream>>>(a);
     else
