@@ -208,33 +208,69 @@ struct Pack<float> {
   }
 };
 
+// A block takes one token at a time: its threads first compact the token's
+// chosen experts (ascending e, warp ballots) into a list of (row, gate) in
+// shared memory, then stride over the row's 16-byte vectors and add the
+// listed rows in that order.
 template <typename T>
 __global__ void __launch_bounds__(256) ec_combine_kernel(EcArgs a) {
   constexpr int V = Pack<T>::n;
+  extern __shared__ int ec_smem[];
+  int* rows = ec_smem;                                        // [N]
+  float* gts = reinterpret_cast<float*>(ec_smem + a.N);       // [N]
+  __shared__ int warp_cnt[8];
+  __shared__ int n_sel;
   const int nvec = a.d / V;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= a.T * nvec) return;
-  const int64_t t = i / nvec;
-  const int v = static_cast<int>(i - t * nvec);
-  float acc[V];
-  if (a.y_shared != nullptr) {
-    Pack<T>::load(static_cast<const uint4*>(a.y_shared)[i], acc);
-  } else {
-#pragma unroll
-    for (int q = 0; q < V; ++q) acc[q] = 0.f;
-  }
-  const int32_t* ch = a.choice + t * a.N;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const uint4* Y = static_cast<const uint4*>(a.y_rows);
-  for (int e = 0; e < a.N; ++e) {
-    const int32_t c = ch[e];
-    if (c <= 0) continue;
-    const float g = a.row_gate[c - 1];
-    float y[V];
-    Pack<T>::load(Y[static_cast<int64_t>(c - 1) * nvec + v], y);
+  const uint4* S = static_cast<const uint4*>(a.y_shared);
+  uint4* O = static_cast<uint4*>(a.out);
+  for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+    const int32_t* ch = a.choice + t * a.N;
+    __syncthreads();  // the previous token's list is no longer read
+    if (threadIdx.x == 0) n_sel = 0;
+    __syncthreads();
+    for (int e0 = 0; e0 < a.N; e0 += 256) {
+      const int e = e0 + threadIdx.x;
+      const int32_t c = e < a.N ? ch[e] : 0;
+      const unsigned m = __ballot_sync(0xffffffffu, c > 0);
+      if (lane == 0) warp_cnt[w] = __popc(m);
+      __syncthreads();
+      int before = n_sel;
+      for (int q = 0; q < w; ++q) before += warp_cnt[q];
+      if (c > 0) {
+        const int pos = before + __popc(m & ((1u << lane) - 1u));
+        rows[pos] = c - 1;
+        gts[pos] = a.row_gate[c - 1];
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int tot = 0;
+        for (int q = 0; q < 8; ++q) tot += warp_cnt[q];
+        n_sel += tot;
+      }
+      __syncthreads();
+    }
+    const int cnt = n_sel;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      float acc[V];
+      if (S != nullptr) {
+        Pack<T>::load(S[t * nvec + v], acc);
+      } else {
 #pragma unroll
-    for (int q = 0; q < V; ++q) acc[q] = fmaf(g, y[q], acc[q]);
+        for (int q = 0; q < V; ++q) acc[q] = 0.f;
+      }
+#pragma unroll 4
+      for (int i = 0; i < cnt; ++i) {
+        float y[V];
+        Pack<T>::load(Y[static_cast<int64_t>(rows[i]) * nvec + v], y);
+        const float g = gts[i];
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] = fmaf(g, y[q], acc[q]);
+      }
+      O[t * nvec + v] = Pack<T>::store(acc);
+    }
   }
-  static_cast<uint4*>(a.out)[i] = Pack<T>::store(acc);
 }
 
 }  // namespace
@@ -261,13 +297,13 @@ cudaError_t launch_ec_select(const EcArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_ec_combine(const EcArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
-  const int vec = a.dtype == MOE_F32 ? 4 : 8;
-  const int64_t total = a.T * (a.d / vec);
-  const unsigned grid = static_cast<unsigned>((total + 255) / 256);
+  const int64_t blocks = static_cast<int64_t>(num_sms()) * 8;
+  const unsigned grid = static_cast<unsigned>(a.T < blocks ? a.T : blocks);
+  const size_t smem = static_cast<size_t>(a.N) * (sizeof(int) + sizeof(float));
   if (a.dtype == MOE_F32)
-    ec_combine_kernel<float><<<grid, 256, 0, stream>>>(a);
+    ec_combine_kernel<float><<<grid, 256, smem, stream>>>(a);
   else
-    ec_combine_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a);
+    ec_combine_kernel<__nv_bfloat16><<<grid, 256, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -12,7 +12,8 @@
 //   partial  one block per 256 tokens: per-token max / normaliser / lse^2 /
 //            entropy (warp per token), then per-expert probability sums in
 //            token order and assignment counts
-//   final    one block: sums the block partials in block order and writes
+//   final    one block: sums the block partials (a warp per expert column,
+//            fixed order) and writes
 //            [L_bal, L_z, entropy, P_0..P_{N-1}, f_0..f_{N-1}]
 #include <math.h>
 
@@ -131,42 +132,57 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
   }
 }
 
+// One block: a warp per expert column (lanes take every 32nd block, in block
+// order, then a fixed butterfly), the same for the two loss sums, and a fixed
+// block reduction for L_bal. Deterministic.
 __global__ void __launch_bounds__(1024) stats_final_kernel(StatsArgs a, int nb) {
   __shared__ float red[32];
+  __shared__ float l2en[2];
   const int N = a.N;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const size_t stride = static_cast<size_t>(2 * N + 2);
   const float invT = 1.f / static_cast<float>(a.T);
   const float invTk = 1.f / (static_cast<float>(a.T) * static_cast<float>(a.k));
-  float local = 0.f;
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+  float local = 0.f;  // lane 0 of each warp: sum of its experts' f_e P_e
+  for (int e = w; e < N; e += nw) {
     float ps = 0.f, cs = 0.f;
-    for (int b = 0; b < nb; ++b) {
-      const float* P = a.partial + static_cast<size_t>(b) * (2 * N + 2);
+    for (int b = lane; b < nb; b += 32) {
+      const float* P = a.partial + static_cast<size_t>(b) * stride;
       ps += P[e];
       cs += P[N + e];
     }
+    ps = warp_sum_f(ps);
+    cs = warp_sum_f(cs);
     const float Pe = ps * invT, fe = cs * invTk;
-    a.out[3 + e] = Pe;
-    a.out[3 + N + e] = fe;
-    local += fe * Pe;
+    if (lane == 0) {
+      a.out[3 + e] = Pe;
+      a.out[3 + N + e] = fe;
+      local += fe * Pe;
+    }
   }
-  // block reduction in a fixed tree order
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  local = warp_sum_f(local);
+  if (w == nw - 1) {
+    float l2 = 0.f, en = 0.f;
+    for (int b = lane; b < nb; b += 32) {
+      const float* P = a.partial + static_cast<size_t>(b) * stride;
+      l2 += P[2 * N];
+      en += P[2 * N + 1];
+    }
+    l2 = warp_sum_f(l2);
+    en = warp_sum_f(en);
+    if (lane == 0) {
+      l2en[0] = l2;
+      l2en[1] = en;
+    }
+  }
   if (lane == 0) red[w] = local;
   __syncthreads();
   if (w == 0) {
-    float v = lane < (blockDim.x >> 5) ? red[lane] : 0.f;
+    float v = lane < nw ? red[lane] : 0.f;
     v = warp_sum_f(v);
     if (lane == 0) {
-      float l2 = 0.f, en = 0.f;
-      for (int b = 0; b < nb; ++b) {
-        const float* P = a.partial + static_cast<size_t>(b) * (2 * N + 2);
-        l2 += P[2 * N];
-        en += P[2 * N + 1];
-      }
       a.out[0] = static_cast<float>(N) * v;
-      a.out[1] = l2 * invT;
-      a.out[2] = en * invT;
+      a.out[1] = l2en[0] * invT;
+      a.out[2] = l2en[1] * invT;
     }
   }
 }
