@@ -221,6 +221,9 @@ moe_status moe_combine(const moe_config* cfg, const void* y_rows,
  *   idx, gate  [T, k] out (as moe_route); counts [N] int32 out or NULL
  *   Ws_*       NULL when cfg->ffn_shared == 0
  *   ws         at least moe_workspace_size(cfg) bytes
+ * Only enqueues work on `stream`: no host synchronisation and no allocation,
+ * so after one eager call (which sets up per-device launch caches) the call
+ * can be captured in a CUDA graph and replayed on the same buffers.
  */
 moe_status moe_forward(const moe_config* cfg, const void* h, const void* W_r,
                        const float* b_r, const float* sel_bias,

@@ -416,3 +416,42 @@ def test_pair_workloads_cover_both_tail_kinds(cuda_lib, name):
     assert c.sum() >= 768 * w.N, "the grouped GEMM would not run on CTA pairs"
     rem = c % 256
     assert ((rem >= 1) & (rem <= 128)).any() and (rem > 128).any(), c.tolist()
+
+
+@pytest.mark.parametrize("name", ["ragged_softmax_top2", "split_router", "pair_shared_ragged_n",
+                                  "switch_top1"])
+def test_forward_replays_from_a_cuda_graph(cuda_lib, name):
+    """moe_forward only enqueues work on its stream (no host synchronisation,
+    no allocation), so after one eager call it can be captured in a CUDA
+    graph; replays give bitwise the eager results, also with new inputs
+    copied into the captured buffers."""
+    w = SMALL[name]
+    cfg = api.config_for(w)
+    inp = gpu_inputs(synth.make_inputs(w, seed=5, device="cpu"))
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    ws = api.alloc_workspace(cfg, "cuda")
+    outs = api.alloc_outputs(cfg, "cuda", tdt)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        api.forward(cfg, inp, outs, ws, s)          # eager call: caches set up
+    torch.cuda.synchronize()
+    eager = {k_: v.clone() for k_, v in outs.items() if v is not None}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        api.forward(cfg, inp, outs, ws, s)
+    for v in outs.values():
+        if v is not None:
+            v.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    for k_, v in eager.items():
+        assert torch.equal(outs[k_], v), f"{k_} differs after graph replay"
+    # new hidden states in the captured buffer: replay equals an eager run on them
+    h2 = gpu_inputs(synth.make_inputs(w, seed=6, device="cpu"))["h"]
+    inp["h"].copy_(h2)
+    g.replay()
+    torch.cuda.synchronize()
+    ref = run_forward(cfg, inp)
+    for k_ in ("out", "idx", "gate"):
+        assert torch.equal(outs[k_], ref[k_]), f"{k_}: replay on new inputs differs"
