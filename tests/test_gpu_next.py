@@ -48,6 +48,17 @@ def test_route_stats_vs_oracle(cuda_lib, T, N, k, score):
     _check_stats(got, ref, N)
 
 
+def test_route_stats_deterministic(cuda_lib):
+    """Fixed summation order: two calls give the same bits (T spans 40 blocks)."""
+    T, N, k = 10000, 96, 4
+    z = synth.random_logits(T, N, seed=7, std=2.0)
+    cfg = api.make_config(T, 8, N, k, 8, score="softmax")
+    idx, _, ws = _route_logits(cfg, z)
+    a = _stats(cfg, z.cuda(), idx, ws)
+    b = _stats(cfg, z.cuda(), idx, ws)
+    assert (a == b).all()
+
+
 def test_route_stats_uniform_closed_form(cuda_lib):
     T, N, k = 512, 16, 2
     z = torch.zeros((T, N), dtype=torch.float32)

@@ -10,10 +10,11 @@
 //   2. scan     counts[e] = sum_b (capped at the capacity when one is set),
 //               offsets = exclusive scan over e, base[e][b] = sum_{b' < b} count[b'][e]
 //               (one warp per expert column, 32 blocks per warp-scan step)
-//   3. permute  per block: per-warp counts, scan over warps, then the rank of
-//               each pair among earlier pairs of the same expert in its warp;
-//               rank = base + warp prefix + in-warp rank; row = offsets[e] + rank,
-//               or inv = -1 when rank >= capacity. Writes row_token and inv.
+//   3. permute  per block: for each warp and expert the mask of lanes holding
+//               it, scan of the masks' counts over warps (plus the block's
+//               base); rank = base + warp prefix + lower lanes holding e;
+//               row = offsets[e] + rank, or inv = -1 when rank >= capacity.
+//               Writes row_token and inv.
 //   4. gather   a block per token at a time, a thread per 16-byte vector of
 //               the row: reads h[t] once, writes it to the token's k rows.
 // The row of (t, e) is offsets[e] + #{t' < t : e in S_t'}, i.e. rows are
@@ -122,10 +123,11 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(DispatchArgs a, int
 __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
   extern __shared__ int sm[];
   const int N = a.N, k = a.k;
-  int* whist = sm;                                   // [kWarps][N]
-  int* sidx = sm + kWarps * N;                       // [kWarps][32][k]
+  unsigned* lanes = reinterpret_cast<unsigned*>(sm);   // [kWarps][N]: lanes holding e
+  int* wbase = sm + kWarps * N;                        // [kWarps][N]: rank base of the warp
+  int* sidx = sm + 2 * kWarps * N;                     // [kWarps][32][k]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < kWarps * N; i += blockDim.x) whist[i] = 0;
+  for (int i = threadIdx.x; i < kWarps * N; i += blockDim.x) lanes[i] = 0u;
   __syncthreads();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kTB + threadIdx.x;
   const bool valid = t < a.T;
@@ -134,32 +136,31 @@ __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
     int e = valid ? a.idx[t * k + j] : -1;
     if (e < 0 || e >= N) e = -1;  // out-of-range indices were flagged by the count pass
     my_idx[j] = e;
-    if (e >= 0) atomicAdd(&whist[warp * N + e], 1);
+    if (e >= 0) atomicOr(&lanes[warp * N + e], 1u << lane);
   }
   __syncthreads();
-  // per expert: exclusive scan over warps, plus the block's rank base (the
-  // number of the expert's pairs in earlier blocks)
+  // per expert: exclusive scan over warps of their pair counts, plus the
+  // block's rank base (the number of the expert's pairs in earlier blocks)
   for (int e = threadIdx.x; e < N; e += blockDim.x) {
     int run = a.block_base[static_cast<size_t>(e) * gridDim.x + blockIdx.x];
     for (int w = 0; w < kWarps; ++w) {
-      const int c = whist[w * N + e];
-      whist[w * N + e] = run;
-      run += c;
+      wbase[w * N + e] = run;
+      run += __popc(lanes[w * N + e]);
     }
   }
   __syncthreads();
+  // A token never repeats an expert, so the pairs of expert e before (t, j)
+  // inside the warp are the lower lanes holding e: rank = warp base + their
+  // count; rows end up ordered by (expert, token).
   if (valid) {
-    const int* wid = sidx + warp * 32 * k;
+    const unsigned below = (1u << lane) - 1u;
     for (int j = 0; j < k; ++j) {
       const int e = my_idx[j];
       if (e < 0) {
         a.inv[t * k + j] = -1;
         continue;
       }
-      int rank = 0;
-      for (int l = 0; l < lane; ++l)
-        for (int jj = 0; jj < k; ++jj) rank += (wid[l * k + jj] == e);
-      rank += whist[warp * N + e];  // position among all of expert e's pairs
+      const int rank = wbase[warp * N + e] + __popc(lanes[warp * N + e] & below);
       if (a.cap_enabled && rank >= a.capacity) {
         a.inv[t * k + j] = -1;  // beyond the expert's capacity: dropped
         continue;
@@ -208,7 +209,7 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
   const int nb = static_cast<int>((a.T + kTB - 1) / kTB);
   dispatch_count_kernel<<<nb, kTB, a.N * sizeof(int), stream>>>(a);
   dispatch_scan_kernel<<<1, 1024, 0, stream>>>(a, nb);
-  const size_t smem = sizeof(int) * (static_cast<size_t>(kWarps) * a.N + kWarps * 32 * a.k);
+  const size_t smem = sizeof(int) * (2 * static_cast<size_t>(kWarps) * a.N + kWarps * 32 * a.k);
   cudaError_t err = cudaFuncSetAttribute(dispatch_permute_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
