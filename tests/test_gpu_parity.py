@@ -37,6 +37,13 @@ SMALL = {
     # more experts than tokens can cover: many empty groups, N > 256
     "many_experts": Workload("many_experts", T=200, d=64, N=300, F=64, k=8, score="sigmoid",
                              bias_zipf_s=1.1),
+    # 256 rows per expert on average, skewed: groups of 2048 and 1401 rows
+    # (16 and 11 m-tiles) beside 14 groups of 329 rows down to 3, shared expert
+    "skewed_groups": Workload("skewed_groups", T=2048, d=192, N=16, F=256, k=2, F_sh=128,
+                              score="sigmoid", bias_zipf_s=1.1, bias_beta=0.5),
+    # top-1 without a shared expert (fused combine), counts 1350 and 368 .. 76
+    "skewed_groups_top1": Workload("skewed_groups_top1", T=4096, d=128, N=16, F=128, k=1,
+                                   score="sigmoid", norm="none", bias_zipf_s=1.1, bias_beta=0.08),
     # few tokens, wide d: the router's logits GEMM splits d into 4 slices
     # whose partial logits the selection adds in order; sigmoid + bias, k=6
     "split_router": Workload("split_router", T=40, d=1024, N=64, F=64, k=6, score="sigmoid",
@@ -149,7 +156,7 @@ def test_small_workload_stagewise_parity(cuda_lib, name):
 
 @pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "tiny_fp32",
                                   "many_experts", "pair_shared_ragged_n", "pair_half_tails",
-                                  "max_experts_topk"])
+                                  "max_experts_topk", "skewed_groups"])
 def test_forward_equals_stages_and_is_deterministic(cuda_lib, name):
     w = SMALL[name]
     cfg = api.config_for(w)
@@ -362,7 +369,8 @@ def test_route_tensor_core_exact_ties(cuda_lib, score, N, k):
     assert (np.abs(z - O.router_logits(to_f64(h), to_f64(W))) <= bound).all()
 
 
-@pytest.mark.parametrize("name", ["switch_top1", "one_expert", "pair_ragged", "pair_mixed_tails"])
+@pytest.mark.parametrize("name", ["switch_top1", "one_expert", "pair_ragged", "pair_mixed_tails",
+                                  "skewed_groups_top1"])
 def test_fused_top1_forward_vs_oracle(cuda_lib, name):
     """Top-1 without a shared expert: moe_forward writes g * E(h) from the down
     pass directly. Checked against the oracle and against the staged path
@@ -384,7 +392,7 @@ def test_fused_top1_forward_vs_oracle(cuda_lib, name):
 
 @pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "many_experts",
                                   "pair_shared_ragged_n", "multi_mtile_ragged_n", "pair_half_tails",
-                                  "pair_mixed_tails"])
+                                  "pair_mixed_tails", "skewed_groups"])
 def test_gather_ffn_equals_dispatched_copy(cuda_lib, name):
     """The grouped GEMM fed by TMA gather4 from h (the moe_forward path) gives
     bitwise the same rows as the one fed by the dispatched copy x_disp."""
