@@ -423,6 +423,8 @@ def bench_ours(args, w):
         "stages_ms": {"route": round(route_ms, 4), "dispatch": round(disp_ms, 4),
                       "grouped_gemm": round(ffn_ms, 4), "combine": round(comb_ms, 4)},
         "next_rows": next_rows,
+        "load": {"rows_max_over_mean": round(float(counts.max()) / max(1e-9, float(counts.mean())), 3),
+                 "idle_experts": int((counts == 0).sum()), "experts": int(w.N)},
         "gpu_launches": kernels_per_forward(w) * args.steps,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_host.numel() * h_host.element_size()),

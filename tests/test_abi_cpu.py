@@ -157,3 +157,30 @@ def test_product_sources_do_not_touch_the_oracle():
                 src = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
                 assert "oracle/" not in src and "moe_oracle" not in src, f
+
+
+def test_nvtx_ranges_enabled_by_environment(api):
+    """MOE_NVTX=1 wraps every entry point in an NVTX range; without a tool
+    attached the ranges are no-ops and the calls behave as before (checked
+    here on the zero-token path, in a fresh process so that the variable is
+    read at the first call)."""
+    import subprocess
+    import sys
+    code = (
+        "import ctypes, sys\n"
+        "sys.path.insert(0, '.')\n"
+        "from top_routing_grouped_bias_b300 import api\n"
+        "lib = api.load()\n"
+        "cfg = api.make_config(0, 64, 4, 2, 64)\n"
+        "fake = ctypes.c_void_p(1 << 20)\n"
+        "n = api.workspace_size(cfg)\n"
+        "s1 = lib.moe_route(ctypes.byref(cfg), fake, fake, None, None, None, None, fake, fake, None, 0, None)\n"
+        "s2 = lib.moe_forward(ctypes.byref(cfg), fake, fake, None, None, fake, fake, fake, None, None,"
+        " None, fake, None, fake, fake, None, fake, n, None)\n"
+        "print(s1, s2)\n")
+    env = dict(os.environ, MOE_NVTX="1")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.split() == [str(api.MOE_OK), str(api.MOE_OK)]

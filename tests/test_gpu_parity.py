@@ -32,6 +32,10 @@ SMALL = {
     "tiny_fp32_shared": synth.WORKLOADS["tiny_fp32"].replace(name="tiny_fp32_shared", F_sh=128,
                                                              score="sigmoid", bias_zipf_s=1.1),
     "single_token": Workload("single_token", T=1, d=64, N=4, F=64, k=2),
+    # odd batch sizes: 3 tokens, and 127 (one short of a tile) with k=3 + bias
+    "three_tokens": Workload("three_tokens", T=3, d=64, N=8, F=64, k=2),
+    "tokens_127": Workload("tokens_127", T=127, d=128, N=8, F=128, k=3, score="sigmoid",
+                           bias_zipf_s=1.1, bias_beta=0.05),
     "one_expert": Workload("one_expert", T=130, d=64, N=1, F=128, k=1),
     "k_equals_N": Workload("k_equals_N", T=64, d=64, N=4, F=64, k=4),
     # more experts than tokens can cover: many empty groups, N > 256

@@ -1,7 +1,9 @@
 // Host side of the C ABI declared in include/moe.h: argument validation,
 // workspace carving and the launch sequence of each entry point.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "internal.h"
@@ -9,6 +11,28 @@
 using namespace moe;
 
 namespace {
+
+// NVTX range around each stage and entry point for timeline tools, enabled
+// by MOE_NVTX=1 in the environment (read once per process); otherwise no
+// NVTX call is made.
+bool nvtx_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_NVTX");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
+}
+struct NvtxRange {
+  bool on;
+  explicit NvtxRange(const char* name) : on(nvtx_enabled()) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~NvtxRange() {
+    if (on) nvtxRangePop();
+  }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -47,6 +71,7 @@ moe_status route_impl(const moe_config* cfg, const void* h, const void* W_r, con
                       const float* sel_bias, const float* logits_in, float* logits_out,
                       int32_t* idx, float* gate, int32_t* status, float* partials,
                       cudaStream_t stream) {
+  NvtxRange nvtx_range("moe.route");
   if (h != nullptr) {
     if (!ok_tensor(h) || !ok_tensor(W_r)) return MOE_ERR_INVALID_ARG;
   } else if (!ok_f32(logits_in)) {
@@ -77,6 +102,7 @@ moe_status dispatch_impl(const moe_config* cfg, const void* h, const int32_t* id
                          int32_t* offsets, int32_t* row_token, int32_t* inv, void* x_disp,
                          void* ws, const WsLayout& L, cudaStream_t stream,
                          int64_t capacity = -1) {
+  NvtxRange nvtx_range("moe.dispatch");
   if (!ok_f32(idx) || !ok_f32(counts) || !ok_f32(offsets) || !ok_f32(row_token) || !ok_f32(inv))
     return MOE_ERR_INVALID_ARG;
   if (x_disp != nullptr && (!ok_tensor(x_disp) || !ok_tensor(h))) return MOE_ERR_INVALID_ARG;
@@ -96,6 +122,7 @@ moe_status ffn_impl(const moe_config* cfg, const void* x_disp, const int32_t* of
                     void* y_shared, void* ws, const WsLayout& L, cudaStream_t stream,
                     const int32_t* scatter_token = nullptr, const float* scatter_gate = nullptr,
                     void* scatter_out = nullptr, const int32_t* gather_rows = nullptr) {
+  NvtxRange nvtx_range("moe.expert_ffn");
   const bool a_ok = gather_rows != nullptr ? ok_tensor(h) && ok_f32(gather_rows) : ok_tensor(x_disp);
   if (!a_ok || !ok_f32(offsets) || !ok_tensor(W_gate) || !ok_tensor(W_up) ||
       !ok_tensor(W_down) || !ok_tensor(y_rows))
@@ -120,6 +147,7 @@ moe_status ffn_impl(const moe_config* cfg, const void* x_disp, const int32_t* of
 
 moe_status combine_impl(const moe_config* cfg, const void* y_rows, const int32_t* inv,
                         const float* gate, const void* y_shared, void* out, cudaStream_t stream) {
+  NvtxRange nvtx_range("moe.combine");
   if (!ok_tensor(y_rows) || !ok_f32(inv) || !ok_f32(gate) || !ok_tensor(out))
     return MOE_ERR_INVALID_ARG;
   if (y_shared != nullptr && !ok_tensor(y_shared)) return MOE_ERR_INVALID_ARG;
@@ -208,6 +236,7 @@ moe_status forward_impl(const moe_config* cfg, int64_t capacity, const void* h, 
                         const void* Ws_up, const void* Ws_down, void* out, float* logits_out,
                         int32_t* idx, float* gate, int32_t* counts, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
+  NvtxRange nvtx_range("moe.forward");
   moe_status s = check_config(cfg);
   if (s != MOE_OK) return s;
   if (!ok_tensor(h) || !ok_tensor(W_r) || !ok_tensor(W_gate) || !ok_tensor(W_up) ||
@@ -259,6 +288,7 @@ moe_status moe_route_grouped(const moe_config* cfg, const moe_group_config* grp,
                              const void* W_r, const float* b_r, const float* sel_bias,
                              const float* logits_in, float* logits_out, int32_t* idx,
                              float* gate, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  NvtxRange nvtx_range("moe.route_grouped");
   moe_status s = check_config(cfg);
   if (s != MOE_OK) return s;
   if (grp == nullptr) return MOE_ERR_INVALID_ARG;
@@ -294,6 +324,7 @@ moe_status moe_route_grouped(const moe_config* cfg, const moe_group_config* grp,
 
 moe_status moe_route_stats(const moe_config* cfg, const float* logits, const int32_t* idx,
                            float* stats, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  NvtxRange nvtx_range("moe.route_stats");
   moe_status s = check_config(cfg);
   if (s != MOE_OK) return s;
   if (!ok_f32(logits) || !ok_f32(idx) || !ok_f32(stats)) return MOE_ERR_INVALID_ARG;
@@ -345,6 +376,7 @@ moe_status moe_forward_expert_choice(const moe_config* cfg, int64_t capacity, co
                                      const void* Ws_up, const void* Ws_down, void* out,
                                      float* logits_out, int32_t* tokens_out, float* gates_out,
                                      void* ws, size_t ws_bytes, cudaStream_t stream) {
+  NvtxRange nvtx_range("moe.forward_expert_choice");
   moe_status s = check_config(cfg);
   if (s != MOE_OK) return s;
   if (capacity < 0 || capacity > cfg->T || capacity * cfg->N > cfg->T * cfg->k)
