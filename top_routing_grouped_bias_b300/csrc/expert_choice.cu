@@ -164,13 +164,17 @@ __global__ void ec_offsets_kernel(int32_t* offsets, int N, int C) {
   for (int e = threadIdx.x; e <= N; e += blockDim.x) offsets[e] = e * C;
 }
 
+// A block copies one picked row at a time (blocks stride over the rows), its
+// threads striding over the row's 16-byte vectors.
 __global__ void __launch_bounds__(256) ec_gather_kernel(EcArgs a, int64_t rows, int nvec) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= rows * nvec) return;
-  const int64_t r = i / nvec;
-  const int v = static_cast<int>(i - r * nvec);
-  const int64_t t = a.row_token[r];
-  static_cast<uint4*>(a.x_disp)[i] = static_cast<const uint4*>(a.h)[t * nvec + v];
+  const uint4* H = static_cast<const uint4*>(a.h);
+  uint4* X = static_cast<uint4*>(a.x_disp);
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int64_t t = a.row_token[r];
+    const uint4* src = H + t * nvec;
+    uint4* dst = X + r * nvec;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) dst[v] = src[v];
+  }
 }
 
 template <typename T>
@@ -289,9 +293,11 @@ cudaError_t launch_ec_select(const EcArgs& a, cudaStream_t stream) {
   const int vec = a.dtype == MOE_F32 ? 4 : 8;
   const int nvec = a.d / vec;
   const int64_t rows = static_cast<int64_t>(a.N) * a.C;
-  if (rows > 0)
-    ec_gather_kernel<<<static_cast<unsigned>((rows * nvec + 255) / 256), 256, 0, stream>>>(a, rows,
-                                                                                            nvec);
+  if (rows > 0) {
+    const int64_t blocks = static_cast<int64_t>(num_sms()) * 8;
+    ec_gather_kernel<<<static_cast<unsigned>(rows < blocks ? rows : blocks), 256, 0, stream>>>(
+        a, rows, nvec);
+  }
   return cudaGetLastError();
 }
 
