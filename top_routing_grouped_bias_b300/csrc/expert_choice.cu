@@ -10,9 +10,10 @@
 //   ec_scores   p = softmax (or sigmoid) of each token's logits, written
 //               transposed [N, T] through a shared-memory tile
 //   ec_select   one block per expert: radix select (4 x 8-bit digits of the
-//               fp32 bit pattern, non-negative keys) finds the C-th largest
-//               score; tokens above it are taken, ties at it go to the lower
-//               token index; a block-wide scan writes the picked tokens in
+//               fp32 bit pattern, non-negative keys; warp-aggregated
+//               histogram counts) finds the C-th largest score; tokens above
+//               it are taken, ties at it go to the lower token index; block
+//               scans over rounds of tokens write the picked tokens in
 //               ascending order to rows [e*C, e*C + C), their gates, and the
 //               token-by-expert choice matrix used by the combine
 //   ec_gather   x_disp[r] = h[row_token[r]] (16-byte vectors)
@@ -68,94 +69,163 @@ __global__ void __launch_bounds__(256) ec_scores_kernel(EcArgs a) {
   }
 }
 
+// Exclusive block scan of two counts at once (blockDim.x = 1024 = 32 warps);
+// also returns the block totals. Uses `ws` [64] of shared memory.
+__device__ __forceinline__ void block_scan2(int g, int q, int& gx, int& qx, int& gt, int& qt,
+                                            int* ws) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int gi = g, qi = q;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int vg = __shfl_up_sync(0xffffffffu, gi, o);
+    const int vq = __shfl_up_sync(0xffffffffu, qi, o);
+    if (lane >= o) {
+      gi += vg;
+      qi += vq;
+    }
+  }
+  if (lane == 31) {
+    ws[w] = gi;
+    ws[32 + w] = qi;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const int vg = ws[lane], vq = ws[32 + lane];
+    int sg = vg, sq = vq;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ug = __shfl_up_sync(0xffffffffu, sg, o);
+      const int uq = __shfl_up_sync(0xffffffffu, sq, o);
+      if (lane >= o) {
+        sg += ug;
+        sq += uq;
+      }
+    }
+    ws[lane] = sg - vg;       // exclusive prefix of the warps
+    ws[32 + lane] = sq - vq;
+    if (lane == 31) {
+      ws[64] = sg;            // totals
+      ws[65] = sq;
+    }
+  }
+  __syncthreads();
+  gx = ws[w] + gi - g;
+  qx = ws[32 + w] + qi - q;
+  gt = ws[64];
+  qt = ws[65];
+  __syncthreads();  // ws is reused by the next call
+}
+
+constexpr int kEcUnroll = 8;  // rounds of keys loaded per thread at once
+
+// One block (1024 threads) per expert.
 __global__ void __launch_bounds__(1024) ec_select_kernel(EcArgs a) {
   __shared__ unsigned int hist[256];
   __shared__ unsigned int s_digit, s_rem;
-  __shared__ int s_gt[1024], s_eq[1024];
+  __shared__ int scan_ws[66];
   const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31;
   const int64_t T = a.T;
   const int C = a.C;
+  if (C == 0) return;
   const float* key_f = a.scores_t + static_cast<int64_t>(e) * T;
   const unsigned int* key = reinterpret_cast<const unsigned int*>(key_f);
-  // ---- radix select of the C-th largest key (non-negative floats order as unsigned) ----
+  // ---- radix select of the C-th largest key (non-negative floats order as
+  // unsigned): 4 passes of 8-bit digits; each warp adds one count per distinct
+  // digit among its lanes (scores cluster, so per-lane atomics would collide) ----
   unsigned int prefix = 0, mask = 0, rem = static_cast<unsigned int>(C);
-  if (C > 0) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-      __syncthreads();
-      for (int64_t t = threadIdx.x; t < T; t += blockDim.x) {
-        const unsigned int k = key[t];
-        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int64_t t0 = 0; t0 < T; t0 += static_cast<int64_t>(blockDim.x) * kEcUnroll) {
+      unsigned int kk[kEcUnroll];
+#pragma unroll
+      for (int u = 0; u < kEcUnroll; ++u) {  // kEcUnroll rounds of loads in flight
+        const int64_t t = t0 + static_cast<int64_t>(u) * blockDim.x + threadIdx.x;
+        kk[u] = t < T ? key[t] : 0u;
       }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        unsigned int cum = 0;
-        int d = 255;
-        for (; d > 0; --d) {
+#pragma unroll
+      for (int u = 0; u < kEcUnroll; ++u) {
+        const int64_t t = t0 + static_cast<int64_t>(u) * blockDim.x + threadIdx.x;
+        const bool in = t < T && (kk[u] & mask) == prefix;
+        const unsigned int digit = in ? (kk[u] >> shift) & 255u : 256u;  // 256: not counted
+        const unsigned int peers = __match_any_sync(0xffffffffu, digit);
+        if (in && lane == __ffs(peers) - 1)
+          atomicAdd(&hist[digit], static_cast<unsigned int>(__popc(peers)));
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // digit holding the rem-th largest: lane l sums bins [8l, 8l + 8), a
+      // suffix scan over lanes (from digit 255 down) finds the bin
+      unsigned int part = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) part += hist[lane * 8 + i];
+      unsigned int suf = part;  // sum over lanes >= lane
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int v = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += v;
+      }
+      const unsigned int above = suf - part;  // keys in bins of higher lanes
+      // the lane whose chunk contains the boundary: above < rem <= above + part
+      const bool mine = above < rem && rem <= suf;
+      if (mine) {
+        unsigned int cum = above;
+        int d = lane * 8 + 7;
+        for (; d > lane * 8; --d) {
           if (cum + hist[d] >= rem) break;
           cum += hist[d];
         }
         s_digit = static_cast<unsigned int>(d);
         s_rem = rem - cum;
       }
-      __syncthreads();
-      prefix |= s_digit << shift;
-      mask |= 255u << shift;
-      rem = s_rem;
-      __syncthreads();
     }
+    __syncthreads();
+    prefix |= s_digit << shift;
+    mask |= 255u << shift;
+    rem = s_rem;
+    __syncthreads();
   }
-  // prefix = key of the C-th largest; rem = ties at it still to take (C > 0)
+  // prefix = key of the C-th largest; rem = ties at it still to take
   const unsigned int thr = prefix;
-  // ---- picked tokens in ascending order: contiguous chunk per thread ----
-  const int64_t chunk = (T + blockDim.x - 1) / blockDim.x;
-  const int64_t lo = threadIdx.x * chunk, hi = lo + chunk < T ? lo + chunk : T;
-  int gt = 0, eq = 0;
-  if (C > 0)
-    for (int64_t t = lo; t < hi; ++t) {
-      const unsigned int k = key[t];
-      gt += k > thr;
-      eq += k == thr;
-    }
-  s_gt[threadIdx.x] = gt;
-  s_eq[threadIdx.x] = eq;
-  __syncthreads();
-  if (threadIdx.x == 0) {  // exclusive scans (1024 entries, once per expert)
-    int rg = 0, re = 0;
-    for (int i = 0; i < static_cast<int>(blockDim.x); ++i) {
-      const int g = s_gt[i], q = s_eq[i];
-      s_gt[i] = rg;
-      s_eq[i] = re;
-      rg += g;
-      re += q;
-    }
-  }
-  __syncthreads();
-  if (C == 0) return;
-  int gbefore = s_gt[threadIdx.x], ebefore = s_eq[threadIdx.x];
   const int take_eq = static_cast<int>(rem);
-  for (int64_t t = lo; t < hi; ++t) {
-    const unsigned int k = key[t];
-    bool pick = false;
-    int pos = 0;
-    if (k > thr) {
-      pick = true;
-      pos = gbefore + min(ebefore, take_eq);
-      ++gbefore;
-    } else if (k == thr) {
-      if (ebefore < take_eq) {
-        pick = true;
-        pos = gbefore + ebefore;
-      }
-      ++ebefore;
+  // ---- picked tokens in ascending order: rounds of blockDim tokens, block
+  // scans of the above-threshold and tie flags give each pick its position ----
+  int g_run = 0, q_run = 0;
+  for (int64_t t0 = 0; t0 < T; t0 += static_cast<int64_t>(blockDim.x) * kEcUnroll) {
+    unsigned int kk[kEcUnroll];
+#pragma unroll
+    for (int u = 0; u < kEcUnroll; ++u) {
+      const int64_t t = t0 + static_cast<int64_t>(u) * blockDim.x + threadIdx.x;
+      kk[u] = t < T ? key[t] : 0u;
     }
-    if (pick) {
-      const int64_t row = static_cast<int64_t>(e) * C + pos;
-      a.row_token[row] = static_cast<int32_t>(t);
-      a.row_gate[row] = key_f[t];
-      a.choice[t * a.N + e] = static_cast<int32_t>(row + 1);
-      if (a.tokens_out) a.tokens_out[row] = static_cast<int32_t>(t);
-      if (a.gates_out) a.gates_out[row] = key_f[t];
+    for (int u = 0; u < kEcUnroll; ++u) {  // rounds in token order
+      const int64_t t = t0 + static_cast<int64_t>(u) * blockDim.x + threadIdx.x;
+      const int g = t < T && kk[u] > thr, q = t < T && kk[u] == thr;
+      int gx, qx, gt, qt;
+      block_scan2(g, q, gx, qx, gt, qt, scan_ws);
+      const int gb = g_run + gx, eb = q_run + qx;
+      bool pick = false;
+      int pos = 0;
+      if (g) {
+        pick = true;
+        pos = gb + min(eb, take_eq);
+      } else if (q && eb < take_eq) {
+        pick = true;
+        pos = gb + eb;
+      }
+      if (pick) {
+        const int64_t row = static_cast<int64_t>(e) * C + pos;
+        const float gv = __uint_as_float(kk[u]);
+        a.row_token[row] = static_cast<int32_t>(t);
+        a.row_gate[row] = gv;
+        a.choice[t * a.N + e] = static_cast<int32_t>(row + 1);
+        if (a.tokens_out) a.tokens_out[row] = static_cast<int32_t>(t);
+        if (a.gates_out) a.gates_out[row] = gv;
+      }
+      g_run += gt;
+      q_run += qt;
     }
   }
 }
