@@ -12,6 +12,7 @@ namespace moe {
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 16;
 constexpr int kDispatchTokensPerBlock = 256;
+constexpr int kStatsTokensPerBlock = 64;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -69,7 +70,8 @@ inline WsLayout ws_layout(const moe_config& c) {
   L.route_part = take(tc_router ? static_cast<size_t>(rs.splits) * T * rs.n_pad * 4 : 0);
   L.end_route = o;
   L.block_base = take(nb * static_cast<size_t>(c.N) * 4);
-  L.stats = take(nb * (2 * static_cast<size_t>(c.N) + 2) * 4);
+  const size_t nbs = (T + kStatsTokensPerBlock - 1) / kStatsTokensPerBlock;
+  L.stats = take(nbs * (2 * static_cast<size_t>(c.N) + 2) * 4);
   L.end_dispatch = o;
   L.act = take(R * static_cast<size_t>(c.ffn) * e);
   L.act_sh = take(T * static_cast<size_t>(c.ffn_shared) * e);

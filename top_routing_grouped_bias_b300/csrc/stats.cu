@@ -9,7 +9,7 @@
 // scores divided by their per-token sum for a sigmoid router.
 //
 // Two launches, deterministic (fixed summation order, integer counts):
-//   partial  one block per 256 tokens: per-token max / normaliser / lse^2 /
+//   partial  one block per 64 tokens: per-token max / normaliser / lse^2 /
 //            entropy (warp per token), then per-expert probability sums in
 //            token order and assignment counts
 //   final    one block: sums the block partials (a warp per expert column,
@@ -22,7 +22,7 @@
 namespace moe {
 namespace {
 
-constexpr int kTok = kDispatchTokensPerBlock;  // 256 tokens per block
+constexpr int kTok = kStatsTokensPerBlock;  // 64 tokens per block
 
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
@@ -93,7 +93,10 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
     }
   }
   __syncthreads();
-  float* P = a.partial + static_cast<size_t>(blockIdx.x) * (2 * N + 2);
+  // row-major [2N + 2][blocks]: each quantity's partials over the blocks
+  // are contiguous for the final reduction
+  const size_t nbk = gridDim.x;
+  float* P = a.partial + blockIdx.x;
   // per-expert probability sums: with few experts several threads share an
   // expert, each summing every ns-th token in order; the slices are then
   // added in slice order (fixed order, deterministic)
@@ -104,10 +107,11 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
     const int sl = threadIdx.x / (256 / ns);
     float acc = 0.f;
     if (e < N && sl < ns) {
-      for (int lt = sl; lt < kTok; lt += ns) {
-        const int64_t t = t0 + lt;
-        if (t >= a.T) break;
-        const float z = a.logits[t * N + e];
+      // tokens of this block, in order; loads of eight of them in flight
+      const int lt_end = a.T - t0 < kTok ? static_cast<int>(a.T - t0) : kTok;
+#pragma unroll 8
+      for (int lt = sl; lt < lt_end; lt += ns) {
+        const float z = a.logits[(t0 + lt) * N + e];
         acc += softmax ? expf(z - s_m[lt]) / s_norm[lt] : 1.f / (1.f + expf(-z)) / s_norm[lt];
       }
     }
@@ -116,19 +120,19 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
     if (threadIdx.x < 256 / ns && e0 + static_cast<int>(threadIdx.x) < N) {
       float tot = 0.f;
       for (int q = 0; q < ns; ++q) tot += s_part[q * (256 / ns) + threadIdx.x];
-      P[e0 + threadIdx.x] = tot;
+      P[(e0 + threadIdx.x) * nbk] = tot;
     }
     __syncthreads();
   }
-  for (int e = threadIdx.x; e < N; e += blockDim.x) P[N + e] = static_cast<float>(s_cnt[e]);
+  for (int e = threadIdx.x; e < N; e += blockDim.x) P[(N + e) * nbk] = static_cast<float>(s_cnt[e]);
   if (threadIdx.x == 0) {
     float l2 = 0.f, en = 0.f;
     for (int lt = 0; lt < kTok; ++lt) {
       l2 += s_lse2[lt];
       en += s_ent[lt];
     }
-    P[2 * N] = l2;
-    P[2 * N + 1] = en;
+    P[(2 * N) * nbk] = l2;
+    P[(2 * N + 1) * nbk] = en;
   }
 }
 
@@ -140,16 +144,28 @@ __global__ void __launch_bounds__(1024) stats_final_kernel(StatsArgs a, int nb) 
   __shared__ float l2en[2];
   const int N = a.N;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const size_t stride = static_cast<size_t>(2 * N + 2);
+  const size_t nbk = static_cast<size_t>(nb);
   const float invT = 1.f / static_cast<float>(a.T);
   const float invTk = 1.f / (static_cast<float>(a.T) * static_cast<float>(a.k));
   float local = 0.f;  // lane 0 of each warp: sum of its experts' f_e P_e
   for (int e = w; e < N; e += nw) {
     float ps = 0.f, cs = 0.f;
-    for (int b = lane; b < nb; b += 32) {
-      const float* P = a.partial + static_cast<size_t>(b) * stride;
-      ps += P[e];
-      cs += P[N + e];
+    const float* pp = a.partial + e * nbk;
+    const float* pc = a.partial + (N + e) * nbk;
+    for (int b0 = lane; b0 < nb; b0 += 256) {
+      // eight of this lane's blocks loaded before they are added, in order
+      float vp[8], vc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int b = b0 + 32 * u;
+        vp[u] = b < nb ? pp[b] : 0.f;
+        vc[u] = b < nb ? pc[b] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        ps += vp[u];
+        cs += vc[u];
+      }
     }
     ps = warp_sum_f(ps);
     cs = warp_sum_f(cs);
@@ -162,10 +178,21 @@ __global__ void __launch_bounds__(1024) stats_final_kernel(StatsArgs a, int nb) 
   }
   if (w == nw - 1) {
     float l2 = 0.f, en = 0.f;
-    for (int b = lane; b < nb; b += 32) {
-      const float* P = a.partial + static_cast<size_t>(b) * stride;
-      l2 += P[2 * N];
-      en += P[2 * N + 1];
+    const float* pl = a.partial + (2 * N) * nbk;
+    const float* pe = a.partial + (2 * N + 1) * nbk;
+    for (int b0 = lane; b0 < nb; b0 += 256) {
+      float vl[8], ve[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int b = b0 + 32 * u;
+        vl[u] = b < nb ? pl[b] : 0.f;
+        ve[u] = b < nb ? pe[b] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        l2 += vl[u];
+        en += ve[u];
+      }
     }
     l2 = warp_sum_f(l2);
     en = warp_sum_f(en);
