@@ -204,14 +204,17 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
   }
 
   // ---- top-k: k rounds of a warp arg-max, lowest index on ties ----
-  uint32_t taken = 0;  // bit i: expert lane + 32 i already selected
+  // bit i of `avail`: expert lane + 32 i can still be taken (not yet taken,
+  // and its group kept)
+  uint32_t avail = 0;
+  for (int i = 0, e = lane; e < N; ++i, e += 32)
+    if (!grouped || ((gkeep >> (e / gs)) & 1u)) avail |= 1u << i;  // masked group: -inf
   int my_sel = -1;     // lane j < k keeps the expert of slot j
   for (int r = 0; r < k; ++r) {
     float best = -INFINITY;
     int best_e = 0x7fffffff;
     for (int i = 0, e = lane; e < N; ++i, e += 32) {
-      if ((taken >> i) & 1u) continue;
-      if (!((gkeep >> (e / gs)) & 1u)) continue;  // masked group (-inf)
+      if (!((avail >> i) & 1u)) continue;
       const float v = sel[e];
       if (v > best || (v == best && e < best_e)) {
         best = v;
@@ -228,7 +231,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
       }
     }
     if (best_e == 0x7fffffff) best_e = 0;  // only reachable with NaN inputs
-    if ((best_e & 31) == lane) taken |= 1u << (best_e >> 5);
+    if ((best_e & 31) == lane) avail &= ~(1u << (best_e >> 5));
     if (lane == r) my_sel = best_e;
   }
 
