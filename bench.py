@@ -214,6 +214,11 @@ class ClockSampler:
             # microseconds the driver spent in each throttle reason during the region
             out["throttle_us"] = {k: round(self.c1[k] - self.c0[k]) for k in self.COUNTERS}
             out["region_s"] = round(self.t1 - self.t0, 3)
+            # a reason whose counter advanced by more than 1% of the region was
+            # active even if no 10 ms sample caught its bit
+            for k, us in out["throttle_us"].items():
+                if us > 0.01 * out["region_s"] * 1e6 and k not in out["reasons"]:
+                    out["reasons"] = sorted(out["reasons"] + [k])
         return out
 
 
