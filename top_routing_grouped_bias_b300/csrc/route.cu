@@ -62,8 +62,12 @@ struct Vec<float> {
   }
 };
 
-// smem per warp: z[N] and (with a bias) q[N].
-template <typename T>
+// One warp per token.  Expert e = lane + 32 i lives in register slot i of
+// its lane (i < EPL, 32 EPL >= N; slots past N hold -inf and are never
+// available).  Shared memory per warp: z[N] (read back for the gates) and,
+// with a bias or groups, q[N] (for a group pass over groups that are not lane
+// segments).
+template <typename T, int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs a) {
   extern __shared__ float route_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -71,10 +75,12 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
   if (t >= a.T) return;
   const int N = a.N, k = a.k;
   const bool has_bias = a.sel_bias != nullptr;
-  float* z = route_smem + static_cast<size_t>(warp) * N * ((has_bias || a.n_group > 1) ? 2 : 1);
+  const bool grouped = a.n_group > 1;
+  float* z = route_smem + static_cast<size_t>(warp) * N * ((has_bias || grouped) ? 2 : 1);
   float* q = z + N;
 
   // ---- logits ----
+  float zr[EPL];
   if (a.h != nullptr) {
     constexpr int V = Vec<T>::n;
     const T* hrow = static_cast<const T*>(a.h) + t * a.d;
@@ -104,64 +110,127 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
           z[e0 + ee] = acc[ee] + (a.b_r != nullptr ? a.b_r[e0 + ee] : 0.f);
       }
     }
-  } else if (a.partials != nullptr) {
-    // slices added in slice order, four loads in flight
-    const size_t slice = static_cast<size_t>(a.T) * a.ld_partial;
-    const float* zp = a.partials + static_cast<size_t>(t) * a.ld_partial;
-    for (int e = lane; e < N; e += 32) {
-      float v = 0.f;
-      for (int sl = 0; sl < a.n_partials; sl += 4) {
-        float w[4];
+    __syncwarp();
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = sl + u < a.n_partials ? zp[(sl + u) * slice + e] : 0.f;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (sl + u < a.n_partials) v += w[u];
-      }
-      z[e] = v + (a.b_r != nullptr ? a.b_r[e] : 0.f);
-    }
+    for (int i = 0; i < EPL; ++i) zr[i] = lane + 32 * i < N ? z[lane + 32 * i] : -INFINITY;
   } else {
-    const float* zin = a.logits_in + t * N;
-    for (int e = lane; e < N; e += 32) z[e] = zin[e];
+    if (a.partials != nullptr) {
+      // slices added in slice order; U slices of every slot in flight
+      constexpr int U = EPL >= 8 ? 1 : 8 / EPL;
+      const size_t slice = static_cast<size_t>(a.T) * a.ld_partial;
+      const float* zp = a.partials + static_cast<size_t>(t) * a.ld_partial + lane;
+      float acc[EPL];
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
+      for (int sl = 0; sl < a.n_partials; sl += U) {
+        float w[EPL][U];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            w[i][u] = lane + 32 * i < N && sl + u < a.n_partials ? zp[(sl + u) * slice + 32 * i] : 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (sl + u < a.n_partials) acc[i] += w[i][u];
+      }
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        zr[i] = e < N ? acc[i] + (a.b_r != nullptr ? a.b_r[e] : 0.f) : -INFINITY;
+      }
+    } else {
+      const float* zin = a.logits_in + t * N;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) zr[i] = lane + 32 * i < N ? zin[lane + 32 * i] : -INFINITY;
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < N) z[lane + 32 * i] = zr[i];
   }
-  __syncwarp();
   if (a.logits_out != nullptr) {
     float* zo = a.logits_out + t * N;
-    for (int e = lane; e < N; e += 32) zo[e] = z[e];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < N) zo[lane + 32 * i] = zr[i];
   }
 
   // ---- softmax statistics (global max, sum of exp) ----
   float m = -INFINITY;
-  for (int e = lane; e < N; e += 32) m = fmaxf(m, z[e]);
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) m = fmaxf(m, zr[i]);
   m = warp_max(m);
+  float ex[EPL];
   float s = 0.f;
   if (a.score == MOE_SCORE_SOFTMAX) {
-    for (int e = lane; e < N; e += 32) s += expf(z[e] - m);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      ex[i] = 0.f;
+      if (lane + 32 * i < N) {
+        ex[i] = expf(zr[i] - m);
+        s += ex[i];
+      }
+    }
     s = warp_sum(s);
   }
 
   // ---- selection score ----
   // with group-limited selection the group scores are sums/maxima of the
   // scores themselves, so q = p (+ bias) is formed even without a bias
-  const bool grouped = a.n_group > 1;
-  const float* sel = z;
+  int gs = N;
+  int m_top = 1;
+  bool seg = false;  // every group is an aligned lane segment of one 32-expert chunk
+  if (grouped) {
+    gs = N / a.n_group;
+    m_top = a.group_rule == 0 ? 1 : a.top_m;
+    seg = 32 % gs == 0 && m_top <= 2;
+  }
+  float sr[EPL];
   if (has_bias || grouped) {
-    for (int e = lane; e < N; e += 32) {
-      const float p = a.score == MOE_SCORE_SOFTMAX ? expf(z[e] - m) / s : 1.f / (1.f + expf(-z[e]));
-      q[e] = p + (has_bias ? a.sel_bias[e] : 0.f);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      sr[i] = -INFINITY;
+      if (e < N) {
+        const float p = a.score == MOE_SCORE_SOFTMAX ? ex[i] / s : 1.f / (1.f + expf(-zr[i]));
+        sr[i] = p + (has_bias ? a.sel_bias[e] : 0.f);
+        if (grouped && !seg) q[e] = sr[i];
+      }
     }
-    __syncwarp();
-    sel = q;
+    if (grouped && !seg) __syncwarp();
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) sr[i] = zr[i];
   }
 
   // ---- group-limited selection: keep the topk_group best groups ----
+  // group score = max, or the sum of the top_m selection scores taken in
+  // descending order; lane g < n_group ends up with group g's score
   uint32_t gkeep = 0xffffffffu;
-  int gs = N;
   if (grouped) {
-    gs = N / a.n_group;
     float gscore = -INFINITY;
-    if (lane < a.n_group) {
-      const float* sg = sel + lane * gs;
+    if (seg) {
+      // the segment's top-2 list by butterfly merges within the segment
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        if (32 * i >= N) break;
+        float t0 = sr[i];
+        float t1 = -INFINITY;
+        for (int o = gs >> 1; o > 0; o >>= 1) {
+          const float u0 = __shfl_xor_sync(0xffffffffu, t0, o);
+          if (m_top == 2) {
+            const float u1 = __shfl_xor_sync(0xffffffffu, t1, o);
+            t1 = fmaxf(fminf(t0, u0), fmaxf(t1, u1));
+          }
+          t0 = fmaxf(t0, u0);
+        }
+        const float sc = a.group_rule == 0 ? t0 : (m_top == 1 ? 0.f + t0 : (0.f + t0) + t1);
+        const float v = __shfl_sync(0xffffffffu, sc, (lane * gs) & 31);
+        if (lane < a.n_group && (lane * gs) >> 5 == i) gscore = v;
+      }
+    } else if (lane < a.n_group) {
+      const float* sg = q + lane * gs;
       if (a.group_rule == 0) {
         for (int i = 0; i < gs; ++i) gscore = fmaxf(gscore, sg[i]);
       } else {
@@ -172,51 +241,59 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
           float v = sg[i];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            if (j < a.top_m && v > tv[j]) {
-              const float t = tv[j];
+            if (j < m_top && v > tv[j]) {
+              const float tt = tv[j];
               tv[j] = v;
-              v = t;
+              v = tt;
             }
           }
         }
         gscore = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (j < a.top_m) gscore += tv[j];
+          if (j < m_top) gscore += tv[j];
       }
     }
-    gkeep = 0;
-    for (int r = 0; r < a.topk_group; ++r) {
-      const bool cand = lane < a.n_group && !((gkeep >> lane) & 1u);
-      float best = cand ? gscore : -INFINITY;
-      int best_g = cand ? lane : 0x7fffffff;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-        const int og = __shfl_xor_sync(0xffffffffu, best_g, o);
-        if (ov > best || (ov == best && og < best_g)) {
-          best = ov;
-          best_g = og;
-        }
-      }
-      if (best_g < 32) gkeep |= 1u << best_g;
+    // group g is kept when fewer than topk_group groups precede it in the
+    // order (score descending, index ascending)
+    int rank = 0;
+    for (int h = 0; h < a.n_group; ++h) {
+      const float sh = __shfl_sync(0xffffffffu, gscore, h);
+      if (sh > gscore || (sh == gscore && h < lane)) ++rank;
     }
+    gkeep = __ballot_sync(0xffffffffu, lane < a.n_group && rank < a.topk_group);
   }
 
   // ---- top-k: k rounds of a warp arg-max, lowest index on ties ----
-  // bit i of `avail`: expert lane + 32 i can still be taken (not yet taken,
-  // and its group kept)
+  // bit i of `avail`: slot i can still be taken (a real expert, not yet
+  // taken, its group kept)
   uint32_t avail = 0;
-  for (int i = 0, e = lane; e < N; ++i, e += 32)
-    if (!grouped || ((gkeep >> (e / gs)) & 1u)) avail |= 1u << i;  // masked group: -inf
+  if (!grouped) {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < N) avail |= 1u << i;
+  } else if (seg) {
+    const int per = 32 / gs, lg = lane / gs;  // group of slot i: i * per + lg
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < N && ((gkeep >> (i * per + lg)) & 1u)) avail |= 1u << i;
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < N && ((gkeep >> (e / gs)) & 1u)) avail |= 1u << i;
+    }
+  }
+  __syncwarp();  // z[] of every lane is visible before the gates read it
   int my_sel = -1;     // lane j < k keeps the expert of slot j
   for (int r = 0; r < k; ++r) {
     float best = -INFINITY;
     int best_e = 0x7fffffff;
-    for (int i = 0, e = lane; e < N; ++i, e += 32) {
-      if (!((avail >> i) & 1u)) continue;
-      const float v = sel[e];
-      if (v > best || (v == best && e < best_e)) {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const float v = sr[i];
+      const int e = lane + 32 * i;
+      if (((avail >> i) & 1u) && (v > best || (v == best && e < best_e))) {
         best = v;
         best_e = e;
       }
@@ -263,6 +340,26 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_warp_kernel(RouteArgs 
   }
 }
 
+template <typename T, int EPL>
+cudaError_t launch_selection(const RouteArgs& a, unsigned grid, size_t smem, cudaStream_t stream) {
+  const cudaError_t err = cudaFuncSetAttribute(
+      route_warp_kernel<T, EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  route_warp_kernel<T, EPL><<<grid, kRouteWarps * 32, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// register slots per lane: the smallest of 1, 2, 4, 8, 16, 32 with 32 EPL >= N
+template <typename T>
+cudaError_t launch_selection(const RouteArgs& a, unsigned grid, size_t smem, cudaStream_t stream) {
+  if (a.N <= 32) return launch_selection<T, 1>(a, grid, smem, stream);
+  if (a.N <= 64) return launch_selection<T, 2>(a, grid, smem, stream);
+  if (a.N <= 128) return launch_selection<T, 4>(a, grid, smem, stream);
+  if (a.N <= 256) return launch_selection<T, 8>(a, grid, smem, stream);
+  if (a.N <= 512) return launch_selection<T, 16>(a, grid, smem, stream);
+  return launch_selection<T, 32>(a, grid, smem, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs& in, cudaStream_t stream) {
@@ -288,19 +385,8 @@ cudaError_t launch_route(const RouteArgs& in, cudaStream_t stream) {
   const bool two = a.sel_bias != nullptr || a.n_group > 1;
   const size_t smem = static_cast<size_t>(kRouteWarps) * a.N * (two ? 2 : 1) * sizeof(float);
   const unsigned grid = static_cast<unsigned>((a.T + kRouteWarps - 1) / kRouteWarps);
-  cudaError_t err;
-  if (a.dtype == MOE_F32) {
-    err = cudaFuncSetAttribute(route_warp_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    route_warp_kernel<float><<<grid, kRouteWarps * 32, smem, stream>>>(a);
-  } else {
-    err = cudaFuncSetAttribute(route_warp_kernel<__nv_bfloat16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    route_warp_kernel<__nv_bfloat16><<<grid, kRouteWarps * 32, smem, stream>>>(a);
-  }
-  return cudaGetLastError();
+  if (a.dtype == MOE_F32) return launch_selection<float>(a, grid, smem, stream);
+  return launch_selection<__nv_bfloat16>(a, grid, smem, stream);
 }
 
 }  // namespace moe
