@@ -121,7 +121,16 @@ def test_grouped_page2_example(cuda_lib):
 @pytest.mark.parametrize("N,k,G,kg,rule,m,score", [
     (64, 8, 8, 4, "topm_sum", 2, "sigmoid"), (64, 6, 8, 3, "max", 1, "softmax"),
     (256, 8, 8, 4, "topm_sum", 2, "sigmoid"), (32, 4, 32, 4, "max", 1, "softmax"),
-    (60, 5, 6, 2, "topm_sum", 3, "softmax")])
+    (60, 5, 6, 2, "topm_sum", 3, "softmax"),
+    # every register-slot count of the selection kernel (1, 2, 4, 8, 16, 32
+    # experts per lane), groups that are lane segments (size dividing 32, at
+    # most top-2 summed) and groups that are not, expert counts that leave a
+    # partial 32-expert chunk
+    (24, 4, 3, 2, "topm_sum", 2, "softmax"), (48, 5, 6, 3, "max", 1, "sigmoid"),
+    (96, 6, 8, 4, "topm_sum", 2, "sigmoid"), (128, 4, 16, 4, "topm_sum", 1, "softmax"),
+    (200, 8, 8, 2, "max", 1, "softmax"), (256, 8, 32, 4, "topm_sum", 2, "softmax"),
+    (512, 8, 16, 4, "topm_sum", 2, "sigmoid"), (768, 12, 8, 3, "topm_sum", 2, "softmax"),
+    (1024, 16, 32, 8, "max", 1, "sigmoid")])
 def test_grouped_given_logits_exact(cuda_lib, N, k, G, kg, rule, m, score):
     T = 700
     z = synth.random_logits(T, N, seed=N * G + k, std=1.5, ties=True)
@@ -150,6 +159,27 @@ def test_grouped_from_hidden_states_with_bias(cuda_lib):
                                  to_f64(inp["sel_bias"]))
     same = (np_i(idx) == S).all(axis=1)
     # fp32 group sums and scores may flip near-ties; everything else is exact
+    assert same.mean() >= 0.99, same.mean()
+    np.testing.assert_allclose(np_f(gate)[same], g[same], atol=1e-6, rtol=0)
+
+
+@pytest.mark.parametrize("N,k,G,kg,rule,m", [(1024, 8, 32, 8, "max", 1),
+                                               (96, 6, 8, 4, "topm_sum", 2),
+                                               (256, 8, 8, 4, "topm_sum", 2),
+                                               (40, 4, 5, 2, "topm_sum", 2)])
+def test_grouped_given_logits_with_bias(cuda_lib, N, k, G, kg, rule, m):
+    """Sigmoid + selection bias with groups, from given logits: the group
+    pass and the selection run on q = p + bias."""
+    T = 600
+    z = synth.random_logits(T, N, seed=N + G, std=1.5)
+    bias = synth.zipf_bias(torch.Generator().manual_seed(N), N, 1.1, 0.3, "cpu")
+    cfg = api.make_config(T, 8, N, k, 8, score="sigmoid")
+    _, idx, gate = _route_grouped(cfg, api.make_group_config(G, kg, rule, m), z=z, bias=bias)
+    rule_o = O.GROUP_MAX if rule == "max" else O.GROUP_TOPM_SUM
+    S, g, _, _ = O.route_grouped(to_f64(z), k, G, kg, rule_o, m, "sigmoid", "selected",
+                                 to_f64(bias))
+    same = (np_i(idx) == S).all(axis=1)
+    # fp32 scores and group sums may flip near-ties; everything else is exact
     assert same.mean() >= 0.99, same.mean()
     np.testing.assert_allclose(np_f(gate)[same], g[same], atol=1e-6, rtol=0)
 
