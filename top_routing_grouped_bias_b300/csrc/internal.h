@@ -71,7 +71,8 @@ inline WsLayout ws_layout(const moe_config& c) {
   L.end_route = o;
   L.block_base = take(nb * static_cast<size_t>(c.N) * 4);
   const size_t nbs = (T + kStatsTokensPerBlock - 1) / kStatsTokensPerBlock;
-  L.stats = take(nbs * (2 * static_cast<size_t>(c.N) + 2) * 4);
+  // block partials [2N + 2][nbs], then the final reduction's ticket counter
+  L.stats = take(nbs * (2 * static_cast<size_t>(c.N) + 2) * 4 + 4);
   L.end_dispatch = o;
   L.act = take(R * static_cast<size_t>(c.ffn) * e);
   L.act_sh = take(T * static_cast<size_t>(c.ffn_shared) * e);
@@ -182,7 +183,8 @@ struct StatsArgs {
   const float* logits;  // [T, N]
   const int32_t* idx;   // [T, k]
   float* out;           // [3 + 2N]
-  float* partial;       // scratch [nb][2N + 2]
+  float* partial;       // scratch [2N + 2][nb], then one uint32 ticket
+  unsigned* ticket;     // set by the launcher: the word after the partials
   int64_t T;
   int32_t N, k, score;
 };

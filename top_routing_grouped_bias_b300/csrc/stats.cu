@@ -9,11 +9,16 @@
 // scores divided by their per-token sum for a sigmoid router.
 //
 // Two launches, deterministic (fixed summation order, integer counts):
-//   partial  one block per 64 tokens: per-token max / normaliser / lse^2 /
-//            entropy (warp per token), then per-expert probability sums in
-//            token order and assignment counts
-//   final    one block: sums the block partials (a warp per expert column,
-//            fixed order) and writes
+//   partial  one block per 64 tokens: the block's logits are staged in shared
+//            memory (64 x N floats, or chunks of 16384 floats for N > 256)
+//            with wide coalesced loads; then per-token max / normaliser /
+//            lse^2 / entropy (warp per token, which also overwrites the token's
+//            staged logits with its probabilities), per-expert probability
+//            sums in token order and assignment counts
+//   final    a warp per quantity column (P_e, counts_e, lse^2, entropy) sums
+//            the block partials in block order; the last block to finish
+//            (an atomic ticket, no waiting) forms L_bal from the written
+//            P_e and f_e in a fixed order, and writes
 //            [L_bal, L_z, entropy, P_0..P_{N-1}, f_0..f_{N-1}]
 #include <math.h>
 
@@ -35,52 +40,117 @@ __device__ __forceinline__ float warp_max_f(float v) {
   return v;
 }
 
-__global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
-  __shared__ float s_m[kTok], s_norm[kTok], s_lse2[kTok], s_ent[kTok];
-  extern __shared__ int s_cnt[];  // [N]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+constexpr int kStageFloats = 16384;  // logits staged per pass: 64 KB
+constexpr int kMaxExpertPasses = 4;  // N <= 1024 experts, 256 per pass
+
+// Tokens of one staged chunk: the whole 64-token block for N <= 256.
+inline int stats_chunk(int N) { return N * kTok <= kStageFloats ? kTok : kStageFloats / N; }
+
+__global__ void __launch_bounds__(256, 4) stats_partial_kernel(StatsArgs a, int chunk) {
+  __shared__ float s_lse2[kTok], s_ent[kTok];
+  __shared__ float s_part[256];
+  extern __shared__ __align__(16) unsigned char stats_smem[];
   const int N = a.N;
+  float* s_z = reinterpret_cast<float*>(stats_smem);  // [chunk][N]
+  int* s_cnt = reinterpret_cast<int*>(stats_smem + static_cast<size_t>(chunk) * N * 4);  // [N]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool softmax = a.score == MOE_SCORE_SOFTMAX;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTok;
+  const int nvalid = a.T - t0 < kTok ? static_cast<int>(a.T - t0) : kTok;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.ticket = 0u;  // read by the final kernel
   for (int e = threadIdx.x; e < N; e += blockDim.x) s_cnt[e] = 0;
-  for (int lt = warp; lt < kTok; lt += 8) {
-    const int64_t t = t0 + lt;
-    if (t >= a.T) {
-      if (lane == 0) { s_m[lt] = 0.f; s_norm[lt] = 1.f; s_lse2[lt] = 0.f; s_ent[lt] = 0.f; }
-      continue;
-    }
-    const float* z = a.logits + t * N;
-    float m = -INFINITY;
-    for (int e = lane; e < N; e += 32) m = fmaxf(m, z[e]);
-    m = warp_max_f(m);
-    float se = 0.f, sze = 0.f, ssig = 0.f;
-    for (int e = lane; e < N; e += 32) {
-      const float ex = expf(z[e] - m);
-      se += ex;
-      sze += ex * (z[e] - m);
-      if (!softmax) ssig += 1.f / (1.f + expf(-z[e]));
-    }
-    se = warp_sum_f(se);
-    sze = warp_sum_f(sze);
-    const float lse = m + logf(se);
-    float norm, ent;
-    if (softmax) {
-      norm = se;
-      ent = logf(se) - sze / se;  // -sum p log p with log p = z - m - log(se)
-    } else {
-      norm = warp_sum_f(ssig);
-      float h = 0.f;
-      for (int e = lane; e < N; e += 32) {
-        const float p = 1.f / (1.f + expf(-z[e])) / norm;
-        if (p > 0.f) h -= p * logf(p);
+  // tokens past T add nothing to the loss sums
+  for (int lt = nvalid + static_cast<int>(threadIdx.x); lt < kTok; lt += blockDim.x) {
+    s_lse2[lt] = 0.f;
+    s_ent[lt] = 0.f;
+  }
+  // per-expert probability sums: with few experts several threads share an
+  // expert, each summing every ns-th token in order; the slices are then
+  // added in slice order (fixed order, deterministic)
+  const int ns = N >= 256 ? 1 : (256 / N < 32 ? 256 / N : 32);
+  const int epp = 256 / ns;  // experts per pass
+  const int sl = threadIdx.x / epp, ecol = threadIdx.x % epp;
+  float acc[kMaxExpertPasses];
+#pragma unroll
+  for (int p = 0; p < kMaxExpertPasses; ++p) acc[p] = 0.f;
+
+  for (int c0 = 0; c0 < nvalid; c0 += chunk) {
+    const int nt = nvalid - c0 < chunk ? nvalid - c0 : chunk;
+    const float* src = a.logits + (t0 + c0) * N;
+    const int nf = nt * N;
+    __syncthreads();  // the previous chunk is fully consumed
+    // ---- stage nt contiguous rows: eight 16-byte loads in flight per thread
+    int done = 0;
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+      const float4* s4 = reinterpret_cast<const float4*>(src);
+      float4* d4 = reinterpret_cast<float4*>(s_z);
+      const int n4 = nf >> 2;
+      for (int i0 = threadIdx.x; i0 < n4; i0 += 256 * 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (i0 + 256 * u < n4) v[u] = s4[i0 + 256 * u];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (i0 + 256 * u < n4) d4[i0 + 256 * u] = v[u];
       }
-      ent = warp_sum_f(h);
+      done = n4 << 2;
     }
-    if (lane == 0) {
-      s_m[lt] = m;
-      s_norm[lt] = norm;
-      s_lse2[lt] = lse * lse;
-      s_ent[lt] = ent;
+    for (int i = done + threadIdx.x; i < nf; i += 256) s_z[i] = src[i];
+    __syncthreads();
+
+    // ---- per-token statistics, a warp per token; each token's row of the
+    // staged tile is then overwritten in place by its probabilities p_e
+    for (int lt = warp; lt < nt; lt += 8) {
+      float* z = s_z + lt * N;
+      float m = -INFINITY;
+      for (int e = lane; e < N; e += 32) m = fmaxf(m, z[e]);
+      m = warp_max_f(m);
+      float se = 0.f, sze = 0.f, ssig = 0.f;
+      for (int e = lane; e < N; e += 32) {
+        const float ze = z[e];
+        const float ex = expf(ze - m);
+        se += ex;
+        sze += ex * (ze - m);
+        if (!softmax) ssig += 1.f / (1.f + expf(-ze));
+        else z[e] = ex;  // the softmax numerator, divided below
+      }
+      se = warp_sum_f(se);
+      sze = warp_sum_f(sze);
+      const float lse = m + logf(se);
+      float norm, ent;
+      if (softmax) {
+        norm = se;
+        ent = logf(se) - sze / se;  // -sum p log p with log p = z - m - log(se)
+        for (int e = lane; e < N; e += 32) z[e] = z[e] / se;
+      } else {
+        norm = warp_sum_f(ssig);
+        float h = 0.f;
+        for (int e = lane; e < N; e += 32) {
+          const float p = 1.f / (1.f + expf(-z[e])) / norm;
+          if (p > 0.f) h -= p * logf(p);
+          z[e] = p;
+        }
+        ent = warp_sum_f(h);
+      }
+      if (lane == 0) {
+        s_lse2[c0 + lt] = lse * lse;
+        s_ent[c0 + lt] = ent;
+      }
+    }
+    __syncthreads();
+
+    // ---- per-expert probability sums over this chunk's tokens, in order
+    // (the p_e written above: the same values as exp(z - m) / se, or the
+    // sigmoid over its token sum)
+#pragma unroll
+    for (int p = 0; p < kMaxExpertPasses; ++p) {
+      const int e = p * epp + ecol;
+      if (e < N && sl < ns) {
+        int lt = c0 + (sl - c0 % ns + ns) % ns;  // first token of slice sl
+#pragma unroll 8
+        for (; lt < c0 + nt; lt += ns) acc[p] += s_z[(lt - c0) * N + e];
+      }
     }
   }
   __syncthreads();
@@ -97,30 +167,15 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
   // are contiguous for the final reduction
   const size_t nbk = gridDim.x;
   float* P = a.partial + blockIdx.x;
-  // per-expert probability sums: with few experts several threads share an
-  // expert, each summing every ns-th token in order; the slices are then
-  // added in slice order (fixed order, deterministic)
-  const int ns = N >= 256 ? 1 : (256 / N < 32 ? 256 / N : 32);
-  __shared__ float s_part[256];
-  for (int e0 = 0; e0 < N; e0 += 256 / ns) {
-    const int e = e0 + threadIdx.x % (256 / ns);
-    const int sl = threadIdx.x / (256 / ns);
-    float acc = 0.f;
-    if (e < N && sl < ns) {
-      // tokens of this block, in order; loads of eight of them in flight
-      const int lt_end = a.T - t0 < kTok ? static_cast<int>(a.T - t0) : kTok;
-#pragma unroll 8
-      for (int lt = sl; lt < lt_end; lt += ns) {
-        const float z = a.logits[(t0 + lt) * N + e];
-        acc += softmax ? expf(z - s_m[lt]) / s_norm[lt] : 1.f / (1.f + expf(-z)) / s_norm[lt];
-      }
-    }
-    s_part[threadIdx.x] = acc;
+#pragma unroll
+  for (int p = 0; p < kMaxExpertPasses; ++p) {
+    if (p * epp >= N) break;
+    s_part[threadIdx.x] = acc[p];
     __syncthreads();
-    if (threadIdx.x < 256 / ns && e0 + static_cast<int>(threadIdx.x) < N) {
+    if (static_cast<int>(threadIdx.x) < epp && p * epp + static_cast<int>(threadIdx.x) < N) {
       float tot = 0.f;
-      for (int q = 0; q < ns; ++q) tot += s_part[q * (256 / ns) + threadIdx.x];
-      P[(e0 + threadIdx.x) * nbk] = tot;
+      for (int q = 0; q < ns; ++q) tot += s_part[q * epp + threadIdx.x];
+      P[(p * epp + threadIdx.x) * nbk] = tot;
     }
     __syncthreads();
   }
@@ -136,91 +191,71 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(StatsArgs a) {
   }
 }
 
-// One block: a warp per expert column (lanes take every 32nd block, in block
-// order, then a fixed butterfly), the same for the two loss sums, and a fixed
-// block reduction for L_bal. Deterministic.
-__global__ void __launch_bounds__(1024) stats_final_kernel(StatsArgs a, int nb) {
-  __shared__ float red[32];
-  __shared__ float l2en[2];
+constexpr int kFinalWarps = 8;
+
+// A warp per column c of the partials: c < N the probability sums of expert
+// c, N <= c < 2N the counts of expert c - N, then lse^2 and entropy. Each lane
+// adds its blocks (lane, lane + 32, ...) in block order, sixteen loads in
+// flight, then a fixed butterfly. The last block to finish forms L_bal from
+// the written P_e and f_e: lane l adds f_e * P_e over e = l, l + 32, ... in
+// order, then the same butterfly. Deterministic.
+__global__ void __launch_bounds__(kFinalWarps * 32) stats_final_kernel(StatsArgs a, int nb) {
+  __shared__ bool s_last;
   const int N = a.N;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kFinalWarps + (threadIdx.x >> 5);
   const size_t nbk = static_cast<size_t>(nb);
   const float invT = 1.f / static_cast<float>(a.T);
   const float invTk = 1.f / (static_cast<float>(a.T) * static_cast<float>(a.k));
-  float local = 0.f;  // lane 0 of each warp: sum of its experts' f_e P_e
-  for (int e = w; e < N; e += nw) {
-    float ps = 0.f, cs = 0.f;
-    const float* pp = a.partial + e * nbk;
-    const float* pc = a.partial + (N + e) * nbk;
-    for (int b0 = lane; b0 < nb; b0 += 256) {
-      // eight of this lane's blocks loaded before they are added, in order
-      float vp[8], vc[8];
+  if (c < 2 * N + 2) {
+    const float* pc = a.partial + c * nbk;
+    float sum = 0.f;
+    for (int b0 = lane; b0 < nb; b0 += 32 * 16) {
+      float v[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const int b = b0 + 32 * u;
-        vp[u] = b < nb ? pp[b] : 0.f;
-        vc[u] = b < nb ? pc[b] : 0.f;
+        v[u] = b < nb ? pc[b] : 0.f;
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        ps += vp[u];
-        cs += vc[u];
-      }
+      for (int u = 0; u < 16; ++u) sum += v[u];
     }
-    ps = warp_sum_f(ps);
-    cs = warp_sum_f(cs);
-    const float Pe = ps * invT, fe = cs * invTk;
+    sum = warp_sum_f(sum);
     if (lane == 0) {
-      a.out[3 + e] = Pe;
-      a.out[3 + N + e] = fe;
-      local += fe * Pe;
+      if (c < N) a.out[3 + c] = sum * invT;                     // P_e
+      else if (c < 2 * N) a.out[3 + c] = sum * invTk;           // f_e
+      else a.out[1 + (c - 2 * N)] = sum * invT;                 // L_z, entropy
     }
   }
-  if (w == nw - 1) {
-    float l2 = 0.f, en = 0.f;
-    const float* pl = a.partial + (2 * N) * nbk;
-    const float* pe = a.partial + (2 * N + 1) * nbk;
-    for (int b0 = lane; b0 < nb; b0 += 256) {
-      float vl[8], ve[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int b = b0 + 32 * u;
-        vl[u] = b < nb ? pl[b] : 0.f;
-        ve[u] = b < nb ? pe[b] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        l2 += vl[u];
-        en += ve[u];
-      }
-    }
-    l2 = warp_sum_f(l2);
-    en = warp_sum_f(en);
-    if (lane == 0) {
-      l2en[0] = l2;
-      l2en[1] = en;
-    }
-  }
-  if (lane == 0) red[w] = local;
+  // the last block to finish sees every other block's writes
+  __threadfence();
   __syncthreads();
-  if (w == 0) {
-    float v = lane < nw ? red[lane] : 0.f;
-    v = warp_sum_f(v);
-    if (lane == 0) {
-      a.out[0] = static_cast<float>(N) * v;
-      a.out[1] = l2en[0] * invT;
-      a.out[2] = l2en[1] * invT;
-    }
-  }
+  if (threadIdx.x == 0) s_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last || threadIdx.x >= 32) return;
+  __threadfence();
+  float local = 0.f;
+  for (int e = lane; e < N; e += 32) local += __ldcg(a.out + 3 + N + e) * __ldcg(a.out + 3 + e);
+  local = warp_sum_f(local);
+  if (lane == 0) a.out[0] = static_cast<float>(N) * local;
 }
 
 }  // namespace
 
-cudaError_t launch_route_stats(const StatsArgs& a, cudaStream_t stream) {
-  if (a.T == 0) return cudaMemsetAsync(a.out, 0, sizeof(float) * (3 + 2 * a.N), stream);
-  const int nb = static_cast<int>((a.T + kTok - 1) / kTok);
-  stats_partial_kernel<<<nb, 256, a.N * sizeof(int), stream>>>(a);
-  stats_final_kernel<<<1, 1024, 0, stream>>>(a, nb);
+cudaError_t launch_route_stats(const StatsArgs& in, cudaStream_t stream) {
+  if (in.T == 0) return cudaMemsetAsync(in.out, 0, sizeof(float) * (3 + 2 * in.N), stream);
+  const int nb = static_cast<int>((in.T + kTok - 1) / kTok);
+  StatsArgs a = in;
+  a.ticket = reinterpret_cast<unsigned*>(a.partial + static_cast<size_t>(nb) * (2 * a.N + 2));
+  const int chunk = stats_chunk(a.N);
+  const size_t smem = static_cast<size_t>(chunk) * a.N * 4 + static_cast<size_t>(a.N) * 4;
+  cudaError_t err = cudaFuncSetAttribute(stats_partial_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  stats_partial_kernel<<<nb, 256, smem, stream>>>(a, chunk);
+  const int cols = 2 * a.N + 2;
+  stats_final_kernel<<<(cols + kFinalWarps - 1) / kFinalWarps, kFinalWarps * 32, 0, stream>>>(a, nb);
   return cudaGetLastError();
 }
 
