@@ -329,9 +329,14 @@ def _ec_check_selection(z64, score, C, tokens, gates):
     return amb
 
 
-@pytest.mark.parametrize("score,shared", [("softmax", False), ("sigmoid", True)])
-def test_expert_choice_layer_vs_oracle(cuda_lib, score, shared):
-    w = Workload("ec", T=700, d=128, N=8, F=128, k=2, F_sh=128 if shared else 0, score=score)
+@pytest.mark.parametrize("score,shared,T,N,k,dtype", [
+    ("softmax", False, 700, 8, 2, "bf16"), ("sigmoid", True, 700, 8, 2, "bf16"),
+    # fp32 with a ragged expert count; 1024 experts (the combine's largest
+    # per-warp choice list)
+    ("sigmoid", True, 600, 300, 4, "f32"), ("sigmoid", False, 512, 1024, 8, "bf16")])
+def test_expert_choice_layer_vs_oracle(cuda_lib, score, shared, T, N, k, dtype):
+    w = Workload("ec", T=T, d=128, N=N, F=128, k=k, F_sh=128 if shared else 0, score=score,
+                 dtype=dtype)
     cfg = api.config_for(w)
     C = w.T * w.k // w.N
     inp = synth.make_inputs(w, seed=8, device="cpu")
@@ -339,7 +344,7 @@ def test_expert_choice_layer_vs_oracle(cuda_lib, score, shared):
     z = np_f(logits)
     o = {k_: to_f64(v) for k_, v in inp.items()}
     amb = _ec_check_selection(z, score, C, tokens, gates)
-    assert amb <= 1
+    assert amb <= max(1, N // 100)   # boundaries within fp32 reach, validated above
     # layer output with the GPU's (validated) picks, oracle fp64 scores and experts
     p = O.scores(O.router_logits(o["h"], o["W_r"]), score)
     ref = np.zeros((w.T, w.d)) if not shared else O.swiglu_expert(o["h"], o["Ws_gate"],
@@ -350,8 +355,8 @@ def test_expert_choice_layer_vs_oracle(cuda_lib, score, shared):
         ye = O.swiglu_expert(o["h"][tk[e]], o["W_gate"][e], o["W_up"][e], o["W_down"][e])
         ref[tk[e]] += p[tk[e], e][:, None] * ye
         mag[tk[e]] += p[tk[e], e][:, None] * np.abs(ye)
-    from gpu_helpers import BF16_TOL, assert_layer_close
-    assert_layer_close(np_f(out), ref, mag, BF16_TOL, "expert choice")
+    from gpu_helpers import assert_layer_close, out_tol
+    assert_layer_close(np_f(out), ref, mag, out_tol(w), "expert choice")
 
 
 def test_expert_choice_ties_and_empty(cuda_lib):

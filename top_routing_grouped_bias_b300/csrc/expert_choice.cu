@@ -282,68 +282,75 @@ struct Pack<float> {
   }
 };
 
-// A block takes one token at a time: its threads first compact the token's
-// chosen experts (ascending e, warp ballots) into a list of (row, gate) in
-// shared memory, then stride over the row's 16-byte vectors and add the
-// listed rows in that order.
+// A warp per token: its lanes compact the token's chosen experts (ascending
+// e, warp ballots) into the warp's list of (row, gate) in shared memory, then
+// stride over the row's 16-byte vectors and add the listed rows in that order.
+// Eight tokens per block, no block-wide barrier: every warp of the SM has its
+// own token's loads in flight.
+constexpr int kEcCombineWarps = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(256) ec_combine_kernel(EcArgs a) {
+__global__ void __launch_bounds__(kEcCombineWarps * 32) ec_combine_kernel(EcArgs a) {
   constexpr int V = Pack<T>::n;
   extern __shared__ int ec_smem[];
-  int* rows = ec_smem;                                        // [N]
-  float* gts = reinterpret_cast<float*>(ec_smem + a.N);       // [N]
-  __shared__ int warp_cnt[8];
-  __shared__ int n_sel;
-  const int nvec = a.d / V;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int* rows = ec_smem + static_cast<size_t>(w) * 2 * a.N;      // [N]
+  float* gts = reinterpret_cast<float*>(rows + a.N);           // [N]
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kEcCombineWarps + w;
+  if (t >= a.T) return;
+  const int nvec = a.d / V;
   const uint4* Y = static_cast<const uint4*>(a.y_rows);
   const uint4* S = static_cast<const uint4*>(a.y_shared);
   uint4* O = static_cast<uint4*>(a.out);
-  for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-    const int32_t* ch = a.choice + t * a.N;
-    __syncthreads();  // the previous token's list is no longer read
-    if (threadIdx.x == 0) n_sel = 0;
-    __syncthreads();
-    for (int e0 = 0; e0 < a.N; e0 += 256) {
-      const int e = e0 + threadIdx.x;
-      const int32_t c = e < a.N ? ch[e] : 0;
-      const unsigned m = __ballot_sync(0xffffffffu, c > 0);
-      if (lane == 0) warp_cnt[w] = __popc(m);
-      __syncthreads();
-      int before = n_sel;
-      for (int q = 0; q < w; ++q) before += warp_cnt[q];
-      if (c > 0) {
-        const int pos = before + __popc(m & ((1u << lane) - 1u));
-        rows[pos] = c - 1;
-        gts[pos] = a.row_gate[c - 1];
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        int tot = 0;
-        for (int q = 0; q < 8; ++q) tot += warp_cnt[q];
-        n_sel += tot;
-      }
-      __syncthreads();
+  const int32_t* ch = a.choice + t * a.N;
+  int cnt = 0;
+  for (int e0 = 0; e0 < a.N; e0 += 32) {
+    const int e = e0 + lane;
+    const int32_t c = e < a.N ? ch[e] : 0;
+    const unsigned m = __ballot_sync(0xffffffffu, c > 0);
+    if (c > 0) {
+      const int pos = cnt + __popc(m & ((1u << lane) - 1u));
+      rows[pos] = c - 1;
+      gts[pos] = a.row_gate[c - 1];
     }
-    const int cnt = n_sel;
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-      float acc[V];
-      if (S != nullptr) {
-        Pack<T>::load(S[t * nvec + v], acc);
+    cnt += __popc(m);
+  }
+  __syncwarp();
+  // each lane's vectors v0, v0 + 32, ... (up to kEcU of them) are loaded
+  // together for every listed row; each element adds the rows in list order
+  constexpr int kEcU = 8;
+  for (int v0 = lane; v0 < nvec; v0 += 32 * kEcU) {
+    float acc[kEcU][V];
+#pragma unroll
+    for (int u = 0; u < kEcU; ++u) {
+      const int v = v0 + 32 * u;
+      if (S != nullptr && v < nvec) {
+        Pack<T>::load(S[t * nvec + v], acc[u]);
       } else {
 #pragma unroll
-        for (int q = 0; q < V; ++q) acc[q] = 0.f;
+        for (int q = 0; q < V; ++q) acc[u][q] = 0.f;
       }
-#pragma unroll 4
-      for (int i = 0; i < cnt; ++i) {
-        float y[V];
-        Pack<T>::load(Y[static_cast<int64_t>(rows[i]) * nvec + v], y);
-        const float g = gts[i];
-#pragma unroll
-        for (int q = 0; q < V; ++q) acc[q] = fmaf(g, y[q], acc[q]);
-      }
-      O[t * nvec + v] = Pack<T>::store(acc);
     }
+    for (int i = 0; i < cnt; ++i) {
+      const int64_t rb = static_cast<int64_t>(rows[i]) * nvec;
+      const float g = gts[i];
+      uint4 raw[kEcU];
+#pragma unroll
+      for (int u = 0; u < kEcU; ++u)
+        if (v0 + 32 * u < nvec) raw[u] = Y[rb + v0 + 32 * u];
+#pragma unroll
+      for (int u = 0; u < kEcU; ++u) {
+        if (v0 + 32 * u < nvec) {
+          float y[V];
+          Pack<T>::load(raw[u], y);
+#pragma unroll
+          for (int q = 0; q < V; ++q) acc[u][q] = fmaf(g, y[q], acc[u][q]);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kEcU; ++u)
+      if (v0 + 32 * u < nvec) O[t * nvec + v0 + 32 * u] = Pack<T>::store(acc[u]);
   }
 }
 
@@ -373,13 +380,20 @@ cudaError_t launch_ec_select(const EcArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_ec_combine(const EcArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
-  const int64_t blocks = static_cast<int64_t>(num_sms()) * 8;
-  const unsigned grid = static_cast<unsigned>(a.T < blocks ? a.T : blocks);
-  const size_t smem = static_cast<size_t>(a.N) * (sizeof(int) + sizeof(float));
-  if (a.dtype == MOE_F32)
-    ec_combine_kernel<float><<<grid, 256, smem, stream>>>(a);
-  else
-    ec_combine_kernel<__nv_bfloat16><<<grid, 256, smem, stream>>>(a);
+  const unsigned grid = static_cast<unsigned>((a.T + kEcCombineWarps - 1) / kEcCombineWarps);
+  const size_t smem = static_cast<size_t>(kEcCombineWarps) * a.N * (sizeof(int) + sizeof(float));
+  cudaError_t err;
+  if (a.dtype == MOE_F32) {
+    err = cudaFuncSetAttribute(ec_combine_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    ec_combine_kernel<float><<<grid, kEcCombineWarps * 32, smem, stream>>>(a);
+  } else {
+    err = cudaFuncSetAttribute(ec_combine_kernel<__nv_bfloat16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    ec_combine_kernel<__nv_bfloat16><<<grid, kEcCombineWarps * 32, smem, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
