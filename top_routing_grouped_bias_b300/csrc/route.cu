@@ -15,6 +15,14 @@
 // in the logit for both softmax and sigmoid, so selection compares logits
 // directly (no rounding of exp can merge two distinct logits). With a bias the
 // selection score is p + bias in fp32.
+//
+// Layout: lane l of the token's warp holds experts l + 32 i in registers
+// (EPL slots, the smallest of 1, 2, 4, ..., 32 with 32 EPL >= N), so every
+// per-expert pass is an unrolled register loop. Group-limited selection
+// ("MoE：router 怎样选 expert", group section): groups of N / n_group
+// consecutive experts; when that size divides 32 a group is an aligned lane
+// segment and its max or top-2 sum comes from butterfly merges inside the
+// segment, otherwise one lane per group scans its group in shared memory.
 #include <cuda_bf16.h>
 #include <math.h>
 
