@@ -49,7 +49,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,   /* bad shape, null or misaligned pointer ([P2] sparse_moe raises on bad shapes) */
-  MOE_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement */
   MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than moe_workspace_size() */
   MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
   MOE_ERR_TIMEOUT = 5,       /* device side: a bounded wait ran out (read via moe_read_status) */
