@@ -266,7 +266,10 @@ moe_status moe_route_grouped(const moe_config* cfg, const moe_group_config* grp,
  *          L_bal = N * sum_i f_i P_i (1 when both are uniform);
  *          L_z = mean over tokens of (log sum_i exp z_ti)^2;
  *          entropy = mean over tokens of -sum_i p_ti log p_ti.
- *   Deterministic (fixed summation order). ws: per-block partial sums. */
+ *   Deterministic (fixed summation order). ws (moe_workspace_size bytes):
+ *   per-block partial sums and the counter that picks the block closing the
+ *   final reduction; calls sharing one workspace must not overlap on the GPU.
+ *   Too small a workspace returns MOE_ERR_WORKSPACE. */
 moe_status moe_route_stats(const moe_config* cfg, const float* logits, const int32_t* idx,
                            float* stats, void* ws, size_t ws_bytes, cudaStream_t stream);
 
