@@ -125,6 +125,20 @@ def test_host_validation_rejects_before_launch(api, lib):
     assert lib.moe_read_status(None, 0, ctypes.byref(v), None) == api.MOE_ERR_INVALID_ARG
 
 
+def test_route_stats_rejects_small_workspace(api, lib):
+    """The statistics need the workspace's partial-sum region and its final
+    counter: anything smaller than moe_workspace_size's dispatch prefix is
+    refused on the host."""
+    fake = ctypes.c_void_p(1 << 20)
+    cfg = _cfg(api, T=1000, N=64, k=4)
+    assert lib.moe_route_stats(ctypes.byref(cfg), fake, fake, fake, None, 0,
+                               None) == api.MOE_ERR_WORKSPACE
+    assert lib.moe_route_stats(ctypes.byref(cfg), fake, fake, fake, fake, 256,
+                               None) == api.MOE_ERR_WORKSPACE
+    assert lib.moe_route_stats(ctypes.byref(cfg), None, fake, fake, fake,
+                               api.workspace_size(cfg), None) == api.MOE_ERR_INVALID_ARG
+
+
 def test_zero_tokens_is_ok_without_launch(api, lib):
     fake = ctypes.c_void_p(1 << 20)
     cfg = _cfg(api, T=0)
