@@ -6,6 +6,7 @@ transposed operand, an overwrite instead of an add) fails at least one test
 here; the mutation tests at the end plant such mistakes in the oracle and
 check that the pins catch them.
 """
+import itertools
 import math
 
 import numpy as np
@@ -599,3 +600,196 @@ def test_expert_choice_layer_vs_dense_mask():
     np.testing.assert_allclose(y, ref, atol=1e-12)
     y0, _, _ = O.moe_forward_expert_choice(h, W_r, Wg, Wu, Wd, 0, shared=sh)
     np.testing.assert_allclose(y0, O.swiglu_expert(h, *sh), atol=1e-12)
+
+
+# ------------------------------------ pins added for the remaining functions ---
+def test_swiglu_act_vs_library_and_closed_form():
+    """SiLU(x W_gate^T) ⊙ (x W_up^T) against torch in fp64, a scalar closed
+    form, and the identity E(x) = act(x) W_down^T ("MOE 专家选择与路由机制" §一)."""
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((11, 7))
+    Wg, Wu, Wd = rng.standard_normal((6, 7)), rng.standard_normal((6, 7)), rng.standard_normal((7, 6))
+    tx, tg, tu = map(torch.from_numpy, (x, Wg, Wu))
+    ref = (Fnn.silu(Fnn.linear(tx, tg)) * Fnn.linear(tx, tu)).numpy()
+    np.testing.assert_allclose(O.swiglu_act(x, Wg, Wu), ref, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(O.swiglu_act(x, Wg, Wu) @ Wd.T, O.swiglu_expert(x, Wg, Wu, Wd),
+                               atol=1e-12, rtol=0)
+    # scalar: x = 2, W_gate = a, W_up = b -> silu(2a) * 2b
+    a, b = 0.7, -1.9
+    got = O.swiglu_act(np.array([[2.0]]), np.array([[a]]), np.array([[b]]))[0, 0]
+    assert abs(got - (2 * a / (1 + math.exp(-2 * a))) * (2 * b)) < 1e-15
+    # the SiLU is on the gate branch only: act(x; a, b) != act(x; b, a)
+    got_sw = O.swiglu_act(np.array([[2.0]]), np.array([[b]]), np.array([[a]]))[0, 0]
+    assert abs(got_sw - got) > 1e-2
+    # SiLU(0) = 0 kills the row whatever the up branch holds
+    assert O.swiglu_act(np.array([[0.0, 1.0]]), np.array([[1.0, 0.0]]), np.array([[0.0, 5.0]]))[0, 0] == 0.0
+
+
+def _group_brute_force(q_row, p_row, k, n_group, topk_group, rule, top_m, norm):
+    """Group-limited routing of one token by enumeration ("MoE：router 怎样选
+    expert" §跨设备时，为什么还要先选组): group scores from sorted lists,
+    the kept groups as the topk_group-subset with the largest score sum
+    (distinct group scores make it unique), then the k-subset of the kept
+    groups' experts with the largest selection-score sum; slots by descending
+    q; gates from the un-biased scores p. Valid only without ties."""
+    N = len(q_row)
+    gs = N // n_group
+    gsc = []
+    for gi in range(n_group):
+        vals = sorted((float(v) for v in q_row[gi * gs:(gi + 1) * gs]), reverse=True)
+        gsc.append(vals[0] if rule == O.GROUP_MAX else sum(vals[:top_m]))
+    kept = max(itertools.combinations(range(n_group), topk_group),
+               key=lambda c: sum(gsc[i] for i in c))
+    cand = [i for gi in kept for i in range(gi * gs, (gi + 1) * gs)]
+    best = max(itertools.combinations(cand, k), key=lambda c: sum(float(q_row[i]) for i in c))
+    S = sorted(best, key=lambda i: -float(q_row[i]))
+    if norm == O.NORM_SELECTED:
+        tot = sum(float(p_row[i]) for i in S)
+        g = [float(p_row[i]) / tot for i in S]
+    else:
+        g = [float(p_row[i]) for i in S]
+    return S, g
+
+
+@pytest.mark.parametrize("score", [O.SOFTMAX, O.SIGMOID])
+@pytest.mark.parametrize("norm", [O.NORM_SELECTED, O.NORM_NONE])
+def test_route_grouped_brute_force_gates_from_unbiased_scores(score, norm):
+    rng = np.random.default_rng(62)
+    for _ in range(150):
+        n_group = int(rng.integers(1, 5)); gs = int(rng.integers(1, 4)); N = n_group * gs
+        kg = int(rng.integers(1, n_group + 1))
+        k = int(rng.integers(1, kg * gs + 1))
+        m = int(rng.integers(1, gs + 1))
+        z = rng.standard_normal((1, N)) * 1.5
+        bias = rng.standard_normal(N) * 0.3
+        for rule in (O.GROUP_MAX, O.GROUP_TOPM_SUM):
+            S, g, p, q = O.route_grouped(z, k, n_group, kg, rule, m, score, norm, bias)
+            # p straight from the definitions, token by token with math
+            if score == O.SOFTMAX:
+                ex = [math.exp(v) for v in z[0]]
+                p_ref = [v / sum(ex) for v in ex]
+            else:
+                p_ref = [1 / (1 + math.exp(-v)) for v in z[0]]
+            q_ref = [p_ref[i] + bias[i] for i in range(N)]
+            S_bf, g_bf = _group_brute_force(q_ref, p_ref, k, n_group, kg, rule, m, norm)
+            assert S[0].tolist() == S_bf
+            np.testing.assert_allclose(g[0], g_bf, atol=1e-14, rtol=0)
+
+
+def test_route_grouped_page2_example_through_route():
+    """The page's two groups [0.90, 0.10 | 0.80, 0.79], top-2, one group kept,
+    through route_grouped: sigmoid scores with logits chosen so that
+    sigma(z) reproduces the printed scores, no bias. Group max keeps group A
+    (gates 0.90/1.00, 0.10/1.00); the top-2 sum keeps group B (0.80/1.59,
+    0.79/1.59)."""
+    gd = load_golden("page2_group_limited_example.json")
+    s = np.array(gd["scores"])
+    z = np.log(s / (1 - s))[None]
+    S, g, p, _ = O.route_grouped(z, gd["k"], 2, 1, O.GROUP_MAX, 2, O.SIGMOID, O.NORM_SELECTED)
+    np.testing.assert_allclose(p[0], s, atol=1e-15)
+    assert S[0].tolist() == [0, 1]
+    np.testing.assert_allclose(g[0], [0.90, 0.10], atol=1e-12)
+    S, g, _, _ = O.route_grouped(z, gd["k"], 2, 1, O.GROUP_TOPM_SUM, 2, O.SIGMOID, O.NORM_SELECTED)
+    assert S[0].tolist() == [2, 3]
+    np.testing.assert_allclose(g[0], [0.80 / 1.59, 0.79 / 1.59], atol=1e-12)
+    # with a bias that lifts expert 3 above expert 2, slot order follows q
+    # but the gates still come from the un-biased p
+    S, g, _, q = O.route_grouped(z, gd["k"], 2, 1, O.GROUP_TOPM_SUM, 2, O.SIGMOID,
+                                 O.NORM_SELECTED, np.array([0.0, 0.0, 0.0, 0.05]))
+    assert S[0].tolist() == [3, 2]
+    np.testing.assert_allclose(g[0], [0.79 / 1.59, 0.80 / 1.59], atol=1e-12)
+
+
+def test_stats_sigmoid_brute_force_nonuniform():
+    """Routing statistics of a sigmoid router on non-uniform logits against a
+    token-by-token computation with math: P_i from sigma(z) divided by its
+    per-token sum (the reading taken for a sigmoid router), f_i the share of
+    the T*k pairs, L_bal = N sum f_i P_i ("MOE 专家选择与路由机制" §五),
+    z-loss from the raw logits, entropy of the normalised scores."""
+    rng = np.random.default_rng(63)
+    T, N, k = 17, 6, 3
+    z = rng.standard_normal((T, N)) * 1.7 + rng.standard_normal(N)[None] * 0.8
+    bias = rng.standard_normal(N) * 0.2
+    S, _, _, _ = O.route(z, k, O.SIGMOID, O.NORM_SELECTED, bias)
+    st = O.routing_stats(z, S, O.SIGMOID, N)
+    P = [0.0] * N; cnt = [0] * N; lz = 0.0; H = 0.0
+    for t in range(T):
+        sig = [1 / (1 + math.exp(-v)) for v in z[t]]
+        tot = sum(sig)
+        lz += math.log(sum(math.exp(v) for v in z[t])) ** 2
+        for i in range(N):
+            pi = sig[i] / tot
+            P[i] += pi / T
+            H -= pi * math.log(pi) / T
+        for j in range(k):
+            cnt[S[t, j]] += 1
+    f = [c / (T * k) for c in cnt]
+    np.testing.assert_allclose(st["P"], P, atol=1e-14)
+    np.testing.assert_allclose(st["f"], f, atol=0)
+    assert abs(st["L_bal"] - N * sum(a * b for a, b in zip(f, P))) < 1e-12
+    assert abs(st["L_z"] - lz / T) < 1e-12
+    assert abs(st["entropy"] - H) < 1e-12
+    assert abs(sum(st["P"]) - 1.0) < 1e-12 and abs(sum(st["f"]) - 1.0) < 1e-15
+
+
+# --------------------------------------- planted mistakes in the new pins ---
+def test_mutation_swiglu_act_branches_swapped(monkeypatch):
+    def bad_act(x, Wg, Wu):
+        x = np.asarray(x, np.float64)
+        return O.silu(x @ np.asarray(Wu).T) * (x @ np.asarray(Wg).T)
+    _run_pins_expect_failure(monkeypatch, "swiglu_act", bad_act,
+                             [test_swiglu_act_vs_library_and_closed_form])
+
+
+def test_mutation_route_grouped_gates_from_biased_scores(monkeypatch):
+    def bad_route_grouped(z, k, n_group, topk_group, group_score=O.GROUP_MAX, top_m=2,
+                          score_kind=O.SOFTMAX, norm=O.NORM_SELECTED, sel_bias=None):
+        p = O.scores(z, score_kind)
+        q = p if sel_bias is None else p + np.asarray(sel_bias, dtype=np.float64)[None, :]
+        S = O.select_topk_grouped(q, k, n_group, topk_group, group_score, top_m)
+        return S, O.gates_from_scores(q, S, norm), p, q          # gates from q
+    _run_pins_expect_failure(
+        monkeypatch, "route_grouped", bad_route_grouped,
+        [lambda: test_route_grouped_brute_force_gates_from_unbiased_scores(O.SIGMOID, O.NORM_SELECTED),
+         test_route_grouped_page2_example_through_route])
+
+
+def test_mutation_group_mask_zero_instead_of_minus_inf(monkeypatch):
+    orig = O.select_topk
+    def bad_grouped(q, k, n_group, topk_group, group_score=O.GROUP_MAX, top_m=2):
+        q = np.asarray(q, dtype=np.float64)
+        T, N = q.shape
+        gs = N // n_group
+        qg = q.reshape(T, n_group, gs)
+        sg = qg.max(axis=-1) if group_score == O.GROUP_MAX else \
+            -np.sort(-qg, axis=-1)[..., :top_m].sum(axis=-1)
+        kept = orig(sg, topk_group)
+        keep = np.zeros((T, n_group)); np.put_along_axis(keep, kept, 1.0, axis=-1)
+        return orig((qg * keep[..., None]).reshape(T, N), k)     # masked to 0
+    _run_pins_expect_failure(
+        monkeypatch, "select_topk_grouped", bad_grouped,
+        [test_grouped_masks_with_minus_infinity_not_zero,
+         lambda: test_route_grouped_brute_force_gates_from_unbiased_scores(O.SIGMOID, O.NORM_SELECTED)])
+
+
+def test_mutation_group_score_sum_of_all_instead_of_top_m(monkeypatch):
+    orig = O.select_topk
+    def bad_grouped(q, k, n_group, topk_group, group_score=O.GROUP_MAX, top_m=2):
+        q = np.asarray(q, dtype=np.float64)
+        T, N = q.shape
+        gs = N // n_group
+        qg = q.reshape(T, n_group, gs)
+        sg = qg.max(axis=-1) if group_score == O.GROUP_MAX else qg.sum(axis=-1)   # all, not top-m
+        kept = orig(sg, topk_group)
+        mask = np.full((T, n_group), -np.inf); np.put_along_axis(mask, kept, 0.0, axis=-1)
+        return orig((qg + mask[..., None]).reshape(T, N), k)
+    _run_pins_expect_failure(
+        monkeypatch, "select_topk_grouped", bad_grouped,
+        [lambda: test_route_grouped_brute_force_gates_from_unbiased_scores(O.SOFTMAX, O.NORM_NONE)])
+
+
+def test_mutation_sigmoid_stats_unnormalised(monkeypatch):
+    def bad_probs(z, score_kind):
+        return O.softmax(z) if score_kind == O.SOFTMAX else O.sigmoid(z)   # not divided by the sum
+    _run_pins_expect_failure(monkeypatch, "router_probabilities", bad_probs,
+                             [test_stats_sigmoid_brute_force_nonuniform])
