@@ -139,22 +139,35 @@ moe_status moe_dispatch(const moe_config* cfg, const void* h, const int32_t* idx
  * fixed memory budget).
  *   Same arguments, layouts and results as moe_dispatch, without the
  *   workspace. The per-block histograms live in a fixed array inside the
- *   library's device image (1 MiB + 256 B, reserved on every GPU that loads
- *   the library until the process exits). Nothing is allocated: no cudaMalloc,
+ *   library's device image (1 MiB, reserved on every GPU that loads the
+ *   library until the process exits). Nothing is allocated: no cudaMalloc,
  *   no cudaFree, no allocating library routine.
  *   Limit: ceil(T / 256) * N <= 262144 (e.g. T <= 65536 with N <= 1024);
  *   larger requests return MOE_ERR_WORKSPACE before anything is launched.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture. The address is cached with the id of the
+ *   device's context: after a device reset the next call looks it up again,
+ *   so make that call before any capture too.
  *   All calls share the one array: calls whose work overlaps on the GPU (on
  *   different streams, or from several host threads) race and corrupt each
  *   other's results. Serialise them. Out-of-range expert indices are skipped
- *   as in moe_dispatch; this variant has no device status read-out.
+ *   as in moe_dispatch, but this variant has no device status word: such a
+ *   call gives counts that sum to fewer than T*k pairs and no other signal.
  */
 moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* h, const int32_t* idx,
                                 int32_t* counts, int32_t* offsets, int32_t* row_token,
                                 int32_t* inv, void* x_disp, cudaStream_t stream);
+
+/* Expert capacity ([P1] §六 Expert Capacity): C = ceil(capacity_factor * T *
+ * k / N), the most (token, slot) pairs one expert keeps. Evaluated on the host
+ * in double precision in that order ((capacity_factor * T) * k, then / N) and
+ * rounded up; writes *capacity. Requires T >= 0, 1 <= k <= N, a finite
+ * capacity_factor >= 0 and a result <= 2^31 (the range moe_dispatch_capacity
+ * accepts); otherwise MOE_ERR_INVALID_ARG and *capacity is left unchanged.
+ * No CUDA call. */
+moe_status moe_expert_capacity(int64_t T, int32_t k, int32_t N, double capacity_factor,
+                               int64_t* capacity);
 
 /* Dispatch with an expert capacity ([P1] §六 Expert Capacity: C =
  * ceil(capacity_factor * T * k / N); tokens beyond it may be dropped, the

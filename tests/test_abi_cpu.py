@@ -198,3 +198,22 @@ def test_nvtx_ranges_enabled_by_environment(api):
                        text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert r.stdout.split() == [str(api.MOE_OK), str(api.MOE_OK)]
+
+
+def test_expert_capacity_through_the_abi_matches_the_oracle(api, lib):
+    """moe_expert_capacity (pure host arithmetic, no GPU needed) gives the
+    oracle's C = ceil(cf * T * k / N) on a grid that includes fractional
+    factors, exact multiples and a factor of zero; invalid inputs are
+    rejected."""
+    import ctypes
+    from oracle import moe_oracle as O
+    for T in (0, 1, 4, 7, 4096, 8192, 65536, 100003):
+        for k, N in ((1, 1), (2, 4), (2, 8), (8, 256), (1, 128), (3, 7), (16, 1024)):
+            for cf in (0.0, 0.5, 1.0, 1.25, 1.5, 2.0, 0.3, 1.1, 3.75):
+                assert api.expert_capacity(T, k, N, cf) == O.expert_capacity(T, k, N, cf), (T, k, N, cf)
+    out = ctypes.c_int64(-5)
+    for args in ((4, 0, 4, 1.0), (4, 5, 4, 1.0), (-1, 2, 4, 1.0), (4, 2, 4, -0.5),
+                 (4, 2, 4, float("nan")), (4, 2, 4, float("inf")), (2 ** 40, 16, 1, 1.0)):
+        assert lib.moe_expert_capacity(*args, ctypes.byref(out)) == api.MOE_ERR_INVALID_ARG, args
+    assert out.value == -5
+    assert lib.moe_expert_capacity(4, 2, 4, 1.0, None) == api.MOE_ERR_INVALID_ARG

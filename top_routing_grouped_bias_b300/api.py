@@ -34,6 +34,7 @@ ENTRY_POINTS = (
     "moe_forward", "moe_read_status", "moe_selftest_wait_timeout", "moe_status_string",
     "moe_dispatch_noalloc", "moe_route_stats", "moe_route_grouped", "moe_dispatch_capacity",
     "moe_forward_capacity", "moe_forward_expert_choice", "moe_expert_ffn_gather",
+    "moe_expert_capacity",
 )
 
 
@@ -93,6 +94,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_forward.argtypes = [cfgp] + [_vp] * 15 + [_vp, _sz, _vp]
     lib.moe_read_status.argtypes = [_vp, _sz, _i32p, _vp]
     lib.moe_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp, _sz, _vp]
+    lib.moe_expert_capacity.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_double, ctypes.POINTER(ctypes.c_int64)]
     lib.moe_status_string.argtypes = [ctypes.c_int32]
     lib.moe_status_string.restype = ctypes.c_char_p
     for name in ENTRY_POINTS:
@@ -215,9 +218,12 @@ def moe_route_grouped(cfg, grp, h, W_r, b_r, sel_bias, logits_in, logits_out, id
 
 
 def expert_capacity(T: int, k: int, N: int, capacity_factor: float) -> int:
-    """C = ceil(capacity_factor * T * k / N)."""
-    import math
-    return int(math.ceil(capacity_factor * T * k / N))
+    """The library's moe_expert_capacity: C = ceil(capacity_factor * T * k / N)."""
+    out = ctypes.c_int64(0)
+    s = load().moe_expert_capacity(int(T), int(k), int(N), float(capacity_factor),
+                                   ctypes.byref(out))
+    _check(s, "moe_expert_capacity")
+    return int(out.value)
 
 
 def moe_dispatch_capacity(cfg, capacity, h, idx, counts, offsets, row_token, inv, x_disp, ws,

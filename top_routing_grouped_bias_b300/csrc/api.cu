@@ -2,6 +2,7 @@
 // workspace carving and the launch sequence of each entry point.
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -445,6 +446,18 @@ moe_status moe_selftest_wait_timeout(uint64_t budget_ns, void* ws, size_t ws_byt
   if (ws == nullptr || ws_bytes < 256 || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
   if (budget_ns > 1000000000ull) budget_ns = 1000000000ull;
   return from_cuda(launch_selftest_wait(static_cast<int32_t*>(ws), budget_ns, stream));
+}
+
+moe_status moe_expert_capacity(int64_t T, int32_t k, int32_t N, double capacity_factor,
+                               int64_t* capacity) {
+  if (capacity == nullptr || T < 0 || N < 1 || k < 1 || k > N) return MOE_ERR_INVALID_ARG;
+  if (!(capacity_factor >= 0.0) || capacity_factor > 1e30) return MOE_ERR_INVALID_ARG;  // NaN too
+  // ((cf * T) * k) / N in double precision, in this order, rounded up
+  const double c = ceil(capacity_factor * static_cast<double>(T) * static_cast<double>(k) /
+                        static_cast<double>(N));
+  if (c > 2147483648.0) return MOE_ERR_INVALID_ARG;
+  *capacity = static_cast<int64_t>(c);
+  return MOE_OK;
 }
 
 const char* moe_status_string(int32_t status) {
