@@ -5,7 +5,15 @@ end-to-end rate through the C ABI with host buffers, and the CPU oracle timed
 on a bounded sample of the same workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--no-cpu-baseline]
+                    [--impl ours|reference] [--no-cpu-baseline] [--configs all|none]
+
+The line's value, config and roofline are those of --workload (default: the
+Mixtral-shaped prefill). Its "configs" block repeats the measurement for every
+named workload: tokens/s and ms per step, the grouped GEMM against the tensor
+peak (or HBM when the batch is weight-bandwidth bound), route / dispatch /
+combine against HBM, and the clocks of each region. Stage times come from
+events recorded between the four stage calls inside one continuous loop of K
+staged steps, so they add up to that loop's step.
 
 N > 1 runs under torchrun, one replica per GPU (tokens are independent, so
 every rank runs its own batch with its own copy of the weights and no
@@ -274,92 +282,91 @@ def cpu_baseline(w, steps: int = 1):
 
 
 # ------------------------------------------------------------ our arm ---
-def bench_ours(args, w):
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    api.load()
+def stage_bytes(w):
+    """Algorithmic HBM bytes of the memory-bound stages of one forward, from
+    the per-token figures: route d*e + 8k (+ the router weight once),
+    dispatch d*e + k*d*e + 8k, combine k*d*e + d*e + 4k (+ d*e for the
+    shared expert's rows)."""
+    e = 4 if w.dtype == "f32" else 2
+    T, d, N, k = w.T, w.d, w.N, w.k
+    return {"route": T * (d * e + 8 * k) + N * d * e,
+            "dispatch": T * (d * e + k * d * e + 8 * k),
+            "combine": T * (k * d * e + d * e + 4 * k) + (T * d * e if w.F_sh else 0)}
+
+
+def measure_workload(args, w, dev, world, local, barrier, headline: bool):
+    """Times one workload: K moe_forward steps (the step), K staged steps
+    (route, dispatch, expert FFN, combine through their entry points, with
+    events between the stages inside one continuous loop), and K steps
+    through the public API with host buffers. Returns the raw figures."""
     cfg = api.config_for(w)
     inp = synth.make_inputs(w, seed=0, device=dev)
     tdt = w.torch_dtype
     ws = api.alloc_workspace(cfg, dev)
     outs = api.alloc_outputs(cfg, dev, tdt, logits=False)
     stream = torch.cuda.current_stream(dev)
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+    K = args.steps
 
     for _ in range(args.warmup):
         api.forward(cfg, inp, outs, ws, stream)
     torch.cuda.synchronize(dev)
     assert api.read_status(ws) == api.MOE_OK
 
-    # ---- device-resident timing ----
+    # ---- the step: K moe_forward calls, device-resident inputs ----
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
         torch.cuda.synchronize(dev)
         ev0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(K):
             api.forward(cfg, inp, outs, ws, stream)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = ev0.elapsed_time(ev1) / K
     assert api.read_status(ws) == api.MOE_OK
-    ms_max = max_over_ranks(ms, world, dev)
-    value = aggregate_rate(w.T * args.steps, world, ms_max * args.steps / 1e3)
-
-    # ---- grouped-GEMM stage alone (both passes), on the same stream ----
     counts = outs["counts"].cpu().numpy()
+
+    # ---- the same layer as its four stage calls, events between them ----
     R = w.T * w.k
     idx, gate = outs["idx"], outs["gate"]
-    st = {n: torch.empty(s, dtype=torch.int32, device=dev) for n, s in
+    st = {n: torch.empty(sz, dtype=torch.int32, device=dev) for n, sz in
           (("counts", (w.N,)), ("offsets", (w.N + 1,)), ("row_token", (R,)), ("inv", (R,)))}
     x_disp = torch.empty((R, w.d), dtype=tdt, device=dev)
     y_rows = torch.empty((R, w.d), dtype=tdt, device=dev)
     y_sh = torch.empty((w.T, w.d), dtype=tdt, device=dev) if w.F_sh else None
-    api.moe_dispatch(cfg, inp["h"], idx, st["counts"], st["offsets"], st["row_token"], st["inv"],
-                     x_disp, ws, stream)
-
-    def ffn():
-        api.moe_expert_ffn(cfg, x_disp, st["offsets"], inp["W_gate"], inp["W_up"], inp["W_down"],
-                           y_rows, inp["h"], inp.get("Ws_gate"), inp.get("Ws_up"),
-                           inp.get("Ws_down"), y_sh, ws, stream)
-
-    def stage_ms(fn, reps):
-        for _ in range(3):
+    out2 = torch.empty((w.T, w.d), dtype=tdt, device=dev)
+    stages = (
+        ("route", lambda: api.moe_route(cfg, inp["h"], inp["W_r"], None, inp["sel_bias"], None,
+                                        None, idx, gate, ws, stream)),
+        ("dispatch", lambda: api.moe_dispatch(cfg, inp["h"], idx, st["counts"], st["offsets"],
+                                              st["row_token"], st["inv"], x_disp, ws, stream)),
+        ("grouped_gemm", lambda: api.moe_expert_ffn(
+            cfg, x_disp, st["offsets"], inp["W_gate"], inp["W_up"], inp["W_down"], y_rows,
+            inp["h"], inp.get("Ws_gate"), inp.get("Ws_up"), inp.get("Ws_down"), y_sh, ws,
+            stream)),
+        ("combine", lambda: api.moe_combine(cfg, y_rows, st["inv"], gate, y_sh, out2, stream)),
+    )
+    for _ in range(3):
+        for _, fn in stages:
             fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        a.record(stream)
-        for _ in range(reps):
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+           for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    t_region = time.perf_counter()
+    for i in range(K):
+        evs[i][0].record(stream)
+        for j, (_, fn) in enumerate(stages):
             fn()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        return a.elapsed_time(b) / reps
-
-    reps = max(args.steps, 20)
-    t_ffn0 = time.perf_counter()
-    ffn_ms = stage_ms(ffn, reps)
-    ffn_region_s = time.perf_counter() - t_ffn0
-    logits_scratch = None
-    route_ms = stage_ms(lambda: api.moe_route(cfg, inp["h"], inp["W_r"], None, inp["sel_bias"],
-                                              None, logits_scratch, idx, gate, ws, stream), reps)
-    disp_ms = stage_ms(lambda: api.moe_dispatch(cfg, inp["h"], idx, st["counts"], st["offsets"],
-                                                st["row_token"], st["inv"], x_disp, ws, stream),
-                       reps)
-    comb_ms = stage_ms(lambda: api.moe_combine(cfg, y_rows, st["inv"], gate, y_sh, outs["out"],
-                                               stream), reps)
+            evs[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    region_s = time.perf_counter() - t_region
     assert api.read_status(ws) == api.MOE_OK
+    stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
+                for j, (name, _) in enumerate(stages)}
+    staged_ms = evs[0][0].elapsed_time(evs[K - 1][-1]) / K
 
-    # ---- end to end through the C ABI with host buffers ----
+    # ---- end to end through the public API with host buffers ----
     # Every step copies its hidden states from pinned host memory and its
     # output back; the copies of neighbouring steps overlap the compute.
     h_hosts = [inp["h"].cpu().pin_memory() for _ in range(2)]
@@ -374,49 +381,134 @@ def bench_ours(args, w):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(pipe.compute)
     pipe.copy_in.wait_event(e0)   # the first copy of the timed region starts after e0
-    for i in range(args.steps):
+    for i in range(K):
         pipe.step(i, h_hosts[i % 2], out_hosts[i % 2])
     pipe.drain()
     e1.record(pipe.compute)
     torch.cuda.synchronize(dev)
     barrier()
     assert api.read_status(pipe.ws) == api.MOE_OK
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
-    e2e_value = aggregate_rate(w.T * args.steps, world, e2e_ms * args.steps / 1e3)
-    h_host = h_hosts[0]
-    out_host = out_hosts[0]
+    e2e_ms = e0.elapsed_time(e1) / K
+    io = {"h2d_bytes_per_step": int(h_hosts[0].numel() * h_hosts[0].element_size()),
+          "d2h_bytes_per_step": int(out_hosts[0].numel() * out_hosts[0].element_size())}
+    del pipe, h_hosts, out_hosts
 
-    next_rows = time_next_rows(w, cfg, inp, ws, stream, dev, stage_ms)
+    next_rows = None
+    if headline:
+        def stage_time(fn, reps):
+            for _ in range(3):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / reps
+        next_rows = time_next_rows(w, cfg, inp, ws, stream, dev, stage_time)
+    del inp, ws, outs, st, x_disp, y_rows, y_sh, out2
+    torch.cuda.empty_cache()
+    return {"ms": max_over_ranks(ms, world, dev),
+            "e2e_ms": max_over_ranks(e2e_ms, world, dev),
+            "stage_ms": {k_: max_over_ranks(v, world, dev) for k_, v in stage_ms.items()},
+            "staged_ms": max_over_ranks(staged_ms, world, dev), "region_s": region_s,
+            "counts": counts, "clocks": clk.summary(), "io": io, "next_rows": next_rows}
 
-    if rank != 0:
-        return None
+
+def summarize(w, m, args, world):
+    """Per-workload figures of the bench line: rates, the grouped GEMM's
+    roofline, the memory-bound stages against HBM, clocks."""
     peaks, peak_src = load_peaks()
+    counts = m["counts"]
     work = workload_work(w)
     gb = gemm_bytes(w, counts)
-    gemm_tflops = work["gemm_flops"] / (ffn_ms * 1e-3) / 1e12
-    gemm_gbs = gb / (ffn_ms * 1e-3) / 1e9
-    tensor_bound = w.T * w.k / max(1, int((counts > 0).sum())) >= 64
-    traffic = traffic_from_profile(w.name)
-    # a kernel timed alone for well under a second runs at burst clocks; a
-    # longer region settles under the power cap (sustained peak)
-    sustained = ffn_region_s > 0.5
+    gemm_ms = m["stage_ms"]["grouped_gemm"]
+    gemm_tflops = work["gemm_flops"] / (gemm_ms * 1e-3) / 1e12
+    gemm_gbs = gb / (gemm_ms * 1e-3) / 1e9
+    touched = max(1, int((counts > 0).sum()))
+    tensor_bound = w.T * w.k / touched >= 64
+    # a region of well under a second runs at burst clocks; a longer one
+    # settles under the power cap (sustained peak)
+    sustained = m["region_s"] > 0.5
     if tensor_bound:
         peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
         if w.dtype == "f32":
             peak = peak / 2.0   # tf32 nominal dense rate is half of bf16
         roof = {"bound": "tensor", "achieved": round(gemm_tflops, 2), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(gemm_tflops / peak, 4), "traffic": traffic}
+                "unit": "TFLOP/s", "frac": round(gemm_tflops / peak, 4),
+                "hbm_frac": round(gemm_gbs / peaks["hbm_gbs"], 4)}
     else:
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(gemm_gbs / peak, 4), "traffic": traffic}
-    roof.update({"kernel": "grouped GEMM pair (gate/up SwiGLU + down), one moe_expert_ffn call",
+                "frac": round(gemm_gbs / peak, 4),
+                "tensor_tflops": round(gemm_tflops, 2)}
+    roof.update({"traffic": traffic_from_profile(w.name),
+                 "kernel": "grouped GEMM pair (gate/up SwiGLU + down), one moe_expert_ffn call",
                  "algorithmic_flops": work["gemm_flops"], "algorithmic_bytes": gb,
-                 "avg_ms": round(ffn_ms, 4),
+                 "avg_ms": round(gemm_ms, 4),
                  "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})"})
+    sb = stage_bytes(w)
+    stages = {}
+    for name in ("route", "dispatch", "grouped_gemm", "combine"):
+        t = m["stage_ms"][name]
+        stages[name] = {"ms": round(t, 4)}
+        if name in sb:
+            gbs = sb[name] / (t * 1e-3) / 1e9
+            stages[name].update({"bytes": sb[name], "GB/s": round(gbs, 1),
+                                 "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)})
+    out = {"tokens_per_s": round(aggregate_rate(w.T * args.steps, world,
+                                                m["ms"] * args.steps / 1e3), 1),
+           "ms_per_step": round(m["ms"], 4),
+           "e2e_tokens_per_s": round(aggregate_rate(w.T * args.steps, world,
+                                                    m["e2e_ms"] * args.steps / 1e3), 1),
+           "shape": {"T": w.T, "d": w.d, "N": w.N, "ffn": w.F, "k": w.k, "ffn_shared": w.F_sh,
+                     "score": w.score, "norm": w.norm, "dtype": w.dtype},
+           "roofline": roof, "stages": stages,
+           "staged_step_ms": round(m["staged_ms"], 4),
+           "load": {"rows_max_over_mean": round(float(counts.max()) / max(1e-9, float(counts.mean())), 3),
+                    "idle_experts": int((counts == 0).sum()), "experts": int(w.N)},
+           "clocks": m["clocks"]}
+    if w.k == 1 and w.F_sh == 0:
+        out["note"] = ("moe_forward fuses the combine into the down pass; the staged steps "
+                       "run it as a separate launch")
+    if not tensor_bound:
+        # weight-bandwidth-bound batch: the whole layer against HBM
+        layer_b = gb + sb["route"] + sb["dispatch"] + sb["combine"]
+        out["layer_hbm"] = {"bytes": layer_b,
+                            "GB/s": round(layer_b / (m["ms"] * 1e-3) / 1e9, 1),
+                            "frac": round(layer_b / (m["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    return out
+
+
+def bench_ours(args, w):
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    api.load()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    m = measure_workload(args, w, dev, world, local, barrier, headline=True)
+    configs = {w.name: summarize(w, m, args, world)}
+    if args.configs == "all":
+        for name, wc in synth.WORKLOADS.items():
+            if name != w.name:
+                configs[name] = summarize(wc, measure_workload(args, wc, dev, world, local, barrier,
+                                                               headline=False), args, world)
+    if rank != 0:
+        return None
+    head = configs[w.name]
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) hidden, N(0,std) weights; no dataset)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "ffn": w.F, "k": w.k,
@@ -424,17 +516,15 @@ def bench_ours(args, w):
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (expert weights %.2f GB per step)"
                          % (3 * w.N * w.d * w.F * (4 if w.dtype == 'f32' else 2) / 1e9)},
-        "roofline": roof,
-        "stages_ms": {"route": round(route_ms, 4), "dispatch": round(disp_ms, 4),
-                      "grouped_gemm": round(ffn_ms, 4), "combine": round(comb_ms, 4)},
-        "next_rows": next_rows,
-        "load": {"rows_max_over_mean": round(float(counts.max()) / max(1e-9, float(counts.mean())), 3),
-                 "idle_experts": int((counts == 0).sum()), "experts": int(w.N)},
+        "roofline": head["roofline"],
+        "stages_ms": {k_: v["ms"] for k_, v in head["stages"].items()},
+        "staged_step_ms": head["staged_step_ms"],
+        "next_rows": m["next_rows"],
+        "load": head["load"],
         "gpu_launches": kernels_per_forward(w) * args.steps,
-        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(h_host.numel() * h_host.element_size()),
-                "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
-        "clocks": clk.summary(),
+        "e2e": {"value": head["e2e_tokens_per_s"], "unit": "tokens/s", **m["io"]},
+        "clocks": head["clocks"],
+        "configs": configs,
     }
     return line
 
@@ -516,6 +606,8 @@ def main(argv=None):
                     choices=list(synth.WORKLOADS) + list(synth.PROFILE_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", default="all", choices=["all", "none"],
+                    help="also time the other named workloads (the 'configs' block)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -11,10 +11,9 @@ Tolerances (derived in the design notes):
   |out - ref| <= 2^-8 (|ref| + E) + E (bf16), ref = the oracle's combine of
   the GPU's own y_rows and gates;
 * layer output and expert rows: bf16 max-abs <= 2e-2 and rel-L2 <= 5e-3;
-  fp32 (tf32 tensor cores) max-abs <= 1e-2 and rel-L2 <= 2e-3. On the small
-  synthetic cases an output element may instead meet the bf16 bound derived
-  in assert_layer_close (outputs of magnitude >= ~2.5 cannot meet 2e-2 after
-  three bf16 roundings); the named workloads use the stated bound alone.
+  fp32 (tf32 tensor cores) max-abs <= 1e-2 and rel-L2 <= 2e-3, on every case;
+* end-to-end selection: at most max_ambiguous(T) tokens may sit within the
+  logit-error margin of a tie (each still checked for validity).
 """
 from __future__ import annotations
 
@@ -28,6 +27,14 @@ from top_routing_grouped_bias_b300.synth import to_f64
 U32 = 2.0 ** -24
 BF16_TOL = dict(max_abs=2e-2, rel_l2=5e-3)
 F32_TOL = dict(max_abs=1e-2, rel_l2=2e-3)
+
+
+def max_ambiguous(T: int) -> int:
+    """Cap on tokens whose top-(k+1) gaps lie within what the measured logit
+    error can move: 3, or one token per thousand on large batches (measured:
+    0 of 4096 on the Mixtral-shaped prefill, 4 of 8192 on the fine-grained
+    workload)."""
+    return max(3, T // 1000)
 
 
 def out_tol(w):
@@ -46,59 +53,6 @@ def assert_close_tol(got, ref, tol, what=""):
     assert max_abs <= tol["max_abs"], f"{what}: max-abs {max_abs:.3e} > {tol['max_abs']}"
     assert rel_l2 <= tol["rel_l2"], f"{what}: rel-L2 {rel_l2:.3e} > {tol['rel_l2']}"
     return max_abs, rel_l2
-
-
-def assert_layer_close(got, ref, mag, tol, what=""):
-    """Layer output check for synthetic cases whose outputs can exceed the
-    range where the stated absolute bound is reachable in bf16. An element
-    passes when it meets the stated max-abs bound OR the bf16 bound derived
-    from the arithmetic: one rounding of the output (2^-8 |ref|) plus one of
-    each bf16 intermediate that enters it (2^-8 of mag = |y_shared| +
-    sum_j g_j |y_j|) plus the bf16 activation (2^-9 mag). rel-L2 must meet
-    the stated bound over the whole tensor."""
-    got = np.asarray(got, np.float64)
-    ref = np.asarray(ref, np.float64)
-    err = np.abs(got - ref)
-    derived = 2.0 ** -8 * (np.abs(ref) + mag) + 2.0 ** -9 * mag + 1e-3
-    bad = err > np.maximum(tol["max_abs"], derived)
-    assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond both bounds, max err {err.max():.3e}"
-    rel_l2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
-    assert rel_l2 <= tol["rel_l2"], f"{what}: rel-L2 {rel_l2:.3e} > {tol['rel_l2']}"
-    return float(err.max()), rel_l2
-
-
-def expert_rows_magnitude(x_rows, offsets, W_gate, W_up, W_down):
-    """sum_j |W_down[i, j]| |act[r, j]| for every dispatched row (oracle act),
-    the scale of the rounding that the bf16 activation passes into y_rows."""
-    mag = np.zeros((x_rows.shape[0], W_down.shape[1]))
-    for e in range(len(offsets) - 1):
-        r0, r1 = int(offsets[e]), int(offsets[e + 1])
-        if r1 > r0:
-            act = O.swiglu_act(x_rows[r0:r1], W_gate[e], W_up[e])
-            mag[r0:r1] = np.abs(act) @ np.abs(np.asarray(W_down[e], np.float64)).T
-    return mag
-
-
-def assert_expert_rows_close(got, ref, mag, tol, what=""):
-    """Expert outputs (y_rows, y_shared) of synthetic cases whose values can
-    exceed the range where the stated absolute bound is reachable in bf16
-    (one rounding at |y| >= 4 is already 2^-8 |y| > 1.5e-2). An element passes
-    when it meets the stated max-abs bound OR the bound derived from the
-    arithmetic: one rounding of y (2^-8 |ref|) plus the bf16 rounding of the
-    activation carried through W_down (2^-8 mag). rel-L2 must meet the stated
-    bound over the whole tensor."""
-    got = np.asarray(got, np.float64)
-    ref = np.asarray(ref, np.float64)
-    assert got.shape == ref.shape, (what, got.shape, ref.shape)
-    if got.size == 0:
-        return 0.0, 0.0
-    err = np.abs(got - ref)
-    derived = 2.0 ** -8 * (np.abs(ref) + mag) + 1e-3
-    bad = err > np.maximum(tol["max_abs"], derived)
-    assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond both bounds, max err {err.max():.3e}"
-    rel_l2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
-    assert rel_l2 <= tol["rel_l2"], f"{what}: rel-L2 {rel_l2:.3e} > {tol['rel_l2']}"
-    return float(err.max()), rel_l2
 
 
 def np_i(t):

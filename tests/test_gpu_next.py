@@ -244,8 +244,10 @@ def test_capacity_dispatch_random_exact(cuda_lib, T, N, k, C):
 
 @pytest.mark.parametrize("cf", [0.5, 1.0, 1.25])
 def test_capacity_layer_vs_oracle(cuda_lib, cf):
+    # W_down at half the named workloads' deviation keeps outputs of order one,
+    # where the stated 2e-2 absolute bound is reachable after bf16 roundings
     w = Workload("cap", T=700, d=128, N=8, F=128, k=2, F_sh=128, score="sigmoid",
-                 bias_zipf_s=1.1, bias_beta=0.5)
+                 bias_zipf_s=1.1, bias_beta=0.5, wd_scale=0.5)
     cfg = api.config_for(w)
     C = api.expert_capacity(w.T, w.k, w.N, cf)
     inp = synth.make_inputs(w, seed=6, device="cpu")
@@ -264,14 +266,12 @@ def test_capacity_layer_vs_oracle(cuda_lib, cf):
     y_rows = O.expert_rows(o["h"][row_token], offsets, o["W_gate"], o["W_up"], o["W_down"])
     ysh = O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"])
     ref = ysh.copy()
-    mag = np.abs(ysh)
     for t in range(w.T):
         for j in range(w.k):
             if inv[t, j] >= 0:
                 ref[t] += g[t, j] * y_rows[inv[t, j]]
-                mag[t] += abs(g[t, j]) * np.abs(y_rows[inv[t, j]])
-    from gpu_helpers import BF16_TOL, assert_layer_close
-    assert_layer_close(np_f(outs["out"]), ref, mag, BF16_TOL, f"capacity cf={cf}")
+    from gpu_helpers import BF16_TOL, assert_close_tol
+    assert_close_tol(np_f(outs["out"]), ref, BF16_TOL, f"capacity cf={cf}")
     dropped = int((inv < 0).sum())
     print(f"cf={cf}: C={C}, dropped {dropped} of {w.T * w.k} pairs")
     if cf < 1:
@@ -336,7 +336,7 @@ def _ec_check_selection(z64, score, C, tokens, gates):
     ("sigmoid", True, 600, 300, 4, "f32"), ("sigmoid", False, 512, 1024, 8, "bf16")])
 def test_expert_choice_layer_vs_oracle(cuda_lib, score, shared, T, N, k, dtype):
     w = Workload("ec", T=T, d=128, N=N, F=128, k=k, F_sh=128 if shared else 0, score=score,
-                 dtype=dtype)
+                 dtype=dtype, wd_scale=0.5 if dtype == "bf16" else 1.0)
     cfg = api.config_for(w)
     C = w.T * w.k // w.N
     inp = synth.make_inputs(w, seed=8, device="cpu")
@@ -349,14 +349,12 @@ def test_expert_choice_layer_vs_oracle(cuda_lib, score, shared, T, N, k, dtype):
     p = O.scores(O.router_logits(o["h"], o["W_r"]), score)
     ref = np.zeros((w.T, w.d)) if not shared else O.swiglu_expert(o["h"], o["Ws_gate"],
                                                                   o["Ws_up"], o["Ws_down"])
-    mag = np.abs(ref)
     tk = np_i(tokens)
     for e in range(w.N):
         ye = O.swiglu_expert(o["h"][tk[e]], o["W_gate"][e], o["W_up"][e], o["W_down"][e])
         ref[tk[e]] += p[tk[e], e][:, None] * ye
-        mag[tk[e]] += p[tk[e], e][:, None] * np.abs(ye)
-    from gpu_helpers import assert_layer_close, out_tol
-    assert_layer_close(np_f(out), ref, mag, out_tol(w), "expert choice")
+    from gpu_helpers import assert_close_tol, out_tol
+    assert_close_tol(np_f(out), ref, out_tol(w), "expert choice")
 
 
 def test_expert_choice_ties_and_empty(cuda_lib):

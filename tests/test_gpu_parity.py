@@ -6,11 +6,10 @@ import pytest
 import torch
 
 from conftest import load_golden
-from gpu_helpers import (BF16_TOL, F32_TOL, assert_close_tol, assert_expert_rows_close,
-                         assert_layer_close, check_combine, expert_rows_magnitude,
-                         check_selection,
-                         e2e_selection_check, gpu_inputs, logit_bound, np_f, np_i, oracle_gates_from_logits,
-                         out_tol, run_forward, run_staged, selection_scores)
+from gpu_helpers import (BF16_TOL, F32_TOL, assert_close_tol, check_combine, check_selection,
+                         e2e_selection_check, gpu_inputs, logit_bound, max_ambiguous, np_f, np_i,
+                         oracle_gates_from_logits, out_tol, run_forward, run_staged,
+                         selection_scores)
 from oracle import moe_oracle as O
 from top_routing_grouped_bias_b300 import api, synth
 from top_routing_grouped_bias_b300.synth import Workload, to_f64
@@ -73,6 +72,12 @@ SMALL = {
     "pair_mixed_tails": Workload("pair_mixed_tails", T=3400, d=256, N=4, F=384, k=1,
                                  score="sigmoid", bias_zipf_s=1.1, bias_beta=0.1),
 }
+# The bf16 cases draw W_down with half the named workloads' standard deviation,
+# so that expert outputs stay below ~2.6 and the layer output below ~2.6: there
+# a bf16 rounding of y (at most 2^-8 |y|) and of the activation carried through
+# W_down leave the stated 2e-2 absolute bound reachable. (With the full
+# deviation, outputs reach ~5 and one rounding alone is up to 2e-2.)
+SMALL = {n: (w.replace(wd_scale=0.5) if w.dtype == "bf16" else w) for n, w in SMALL.items()}
 
 
 def oracle_inputs(inp):
@@ -81,8 +86,7 @@ def oracle_inputs(inp):
 
 def reference_layer(w, o, idx_gpu):
     """Oracle layer output in fp64 with the GPU's (validated) selection:
-    gates from the oracle's own fp64 logits, experts and combine in fp64.
-    Also returns the magnitude |y_shared| + sum_j g_j |y_j| per element."""
+    gates from the oracle's own fp64 logits, experts and combine in fp64."""
     z = O.router_logits(o["h"], o["W_r"])
     p = O.scores(z, w.score)
     g = O.gates_from_scores(p, idx_gpu, w.norm)
@@ -91,8 +95,7 @@ def reference_layer(w, o, idx_gpu):
     ysh = None
     if w.F_sh > 0:
         ysh = O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"])
-    mag = O.combine(np.abs(y_rows), inv, np.abs(g), None if ysh is None else np.abs(ysh))
-    return O.combine(y_rows, inv, g, ysh), mag
+    return O.combine(y_rows, inv, g, ysh)
 
 
 @pytest.mark.parametrize("name", list(SMALL))
@@ -118,7 +121,7 @@ def test_small_workload_stagewise_parity(cuda_lib, name):
     n_amb = e2e_selection_check(idx, z_ref, z_gpu, w.score, o["sel_bias"], w.k,
                                 f"{name} end to end")
     print(f"{name}: {n_amb} of {w.T} tokens within the logit-error margin of a tie")
-    assert n_amb <= max(3, w.T // 10), n_amb
+    assert n_amb <= max_ambiguous(w.T), n_amb
 
     # ---- gates: oracle fed the GPU's logits and indices ----
     g_ref = oracle_gates_from_logits(z_gpu, idx, w.score, w.norm)
@@ -135,27 +138,17 @@ def test_small_workload_stagewise_parity(cuda_lib, name):
     # ---- expert rows and shared expert ----
     x_rows = o["h"][row_token]
     y_ref = O.expert_rows(x_rows, offsets, o["W_gate"], o["W_up"], o["W_down"])
-    if w.dtype == "f32":
-        assert_close_tol(np_f(r["y_rows"]), y_ref, out_tol(w), f"{name} y_rows")
-    else:
-        mag = expert_rows_magnitude(x_rows, offsets, o["W_gate"], o["W_up"], o["W_down"])
-        assert_expert_rows_close(np_f(r["y_rows"]), y_ref, mag, out_tol(w), f"{name} y_rows")
+    assert_close_tol(np_f(r["y_rows"]), y_ref, out_tol(w), f"{name} y_rows")
     if w.F_sh > 0:
         ysh_ref = O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"])
-        if w.dtype == "f32":
-            assert_close_tol(np_f(r["y_sh"]), ysh_ref, out_tol(w), f"{name} y_shared")
-        else:
-            mag_sh = expert_rows_magnitude(o["h"], np.array([0, w.T]), o["Ws_gate"][None],
-                                           o["Ws_up"][None], o["Ws_down"][None])
-            assert_expert_rows_close(np_f(r["y_sh"]), ysh_ref, mag_sh, out_tol(w),
-                                     f"{name} y_shared")
+        assert_close_tol(np_f(r["y_sh"]), ysh_ref, out_tol(w), f"{name} y_shared")
 
     # ---- combine: one rounding of the GPU's own terms ----
     check_combine(r, cfg, f"{name} combine")
 
     # ---- whole layer ----
-    out_ref, mag = reference_layer(w, o, idx)
-    assert_layer_close(np_f(r["out"]), out_ref, mag, out_tol(w), f"{name} out")
+    out_ref = reference_layer(w, o, idx)
+    assert_close_tol(np_f(r["out"]), out_ref, out_tol(w), f"{name} out")
 
 
 @pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "tiny_fp32",
@@ -184,7 +177,7 @@ def test_forward_matches_dense_masked_oracle(cuda_lib):
                                            w.k, shared=(o["Ws_gate"], o["Ws_up"], o["Ws_down"]))
     n_amb = e2e_selection_check(np_i(r["idx"]), z, np_f(r["logits"]), w.score, None, w.k,
                                 "dense")
-    assert n_amb <= 3
+    assert n_amb == 0
     assert_close_tol(np_f(r["out"]), y_dense, BF16_TOL, "dense masked")
 
 
@@ -390,8 +383,8 @@ def test_fused_top1_forward_vs_oracle(cuda_lib, name):
     fa, fs = np_f(a["out"]), np_f(s["out"])
     assert (np.abs(fa - fs) <= 2.0 ** -7 * np.abs(fs) + 1e-6).all()
     o = oracle_inputs(inp)
-    out_ref, mag = reference_layer(w, o, np_i(a["idx"]))
-    assert_layer_close(fa, out_ref, mag, out_tol(w), f"{name} fused top-1")
+    out_ref = reference_layer(w, o, np_i(a["idx"]))
+    assert_close_tol(fa, out_ref, out_tol(w), f"{name} fused top-1")
 
 
 @pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "many_experts",

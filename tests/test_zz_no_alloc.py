@@ -14,7 +14,8 @@ from top_routing_grouped_bias_b300 import api
 
 def _case(T, N, k, d, seed):
     gen = torch.Generator().manual_seed(seed)
-    idx = torch.stack([torch.randperm(N, generator=gen)[:k] for _ in range(T)]).to(torch.int32)
+    # k distinct experts per token: the k largest of N seeded uniforms
+    idx = torch.rand((T, N), generator=gen).topk(k, dim=1).indices.to(torch.int32)
     h = torch.randn((T, d), generator=gen).to(torch.bfloat16)
     return idx, h
 
@@ -34,22 +35,28 @@ def test_noalloc_dispatch_matches_workspace_dispatch_on_consecutive_calls():
         pytest.fail("GPU test run without a visible CUDA device")
     api.load()
     dev = "cuda"
-    # two calls in a row with different shapes: the second reuses the array
-    # the first one filled
-    for T, N, k, d, seed in ((5000, 256, 8, 64, 1), (777, 1024, 4, 128, 2)):
+    # calls in a row with different shapes, each reusing the array the one
+    # before filled: the last fills the array exactly (ceil(65536 / 256) *
+    # 1024 = 262144 entries), the third skips the row gather (x_disp NULL)
+    cases = ((5000, 256, 8, 64, 1, True), (777, 1024, 4, 128, 2, True),
+             (3000, 64, 6, 32, 3, False), (65536, 1024, 2, 16, 4, True))
+    for T, N, k, d, seed, gather in cases:
         cfg = api.make_config(T, d, N, k, 64)
         idx, h = _case(T, N, k, d, seed)
         idx, h = idx.to(dev), h.to(dev)
         ref = _buffers(cfg, dev)
         ws = api.alloc_workspace(cfg, dev)
         api.moe_dispatch(cfg, h, idx, ref["counts"], ref["offsets"], ref["row_token"],
-                         ref["inv"], ref["x_disp"], ws)
+                         ref["inv"], ref["x_disp"] if gather else None, ws)
         got = _buffers(cfg, dev)
         api.moe_dispatch_noalloc(cfg, h, idx, got["counts"], got["offsets"], got["row_token"],
-                                 got["inv"], got["x_disp"])
+                                 got["inv"], got["x_disp"] if gather else None)
         torch.cuda.synchronize()
         for key in ref:
             assert torch.equal(got[key], ref[key]), f"{key} differs (T={T}, N={N}, k={k})"
+        if not gather:
+            assert not got["x_disp"].any(), "x_disp written although it was not passed"
+        assert int(got["counts"].sum()) == T * k
 
 
 def test_noalloc_dispatch_rejects_sizes_beyond_its_scratch():

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kTB) dispatch_count_kernel(DispatchArgs a) {
       const int e = a.idx[t * a.k + j];
       if (e >= 0 && e < a.N)
         atomicAdd(&hist[e], 1);
-      else
+      else if (a.status != nullptr)
         atomicCAS(a.status, 0, MOE_ERR_DEVICE_CHECK);
     }
   }

@@ -23,7 +23,8 @@ switch_top1            65536  2048  128  768    1   0      softmax   none
 
 Distributions: h ~ N(0, 1); W_r ~ N(0, wr_std); expert weights
 ~ N(0, 1/sqrt(fan_in)) with fan_in = d for W_gate / W_up and F for W_down
-(the second parameter is the standard deviation). fine_grained_shared adds a
+(the second parameter is the standard deviation; ``wd_scale``, 1.0 for the
+named workloads, multiplies W_down's). fine_grained_shared adds a
 per-expert selection bias with a Zipf(s = 1.1) profile:
 bias_i = beta * r_i ** -1.1 with r a seeded random permutation of 1..N and
 beta = 4.0, which leaves several experts with no tokens.
@@ -57,6 +58,10 @@ class Workload:
     wr_std: float = 0.02
     bias_zipf_s: Optional[float] = None
     bias_beta: float = 4.0
+    # multiplier on the standard deviation of W_down (and the shared W_down);
+    # the named workloads keep 1.0, small test cases may draw smaller
+    # down-projection weights so that their outputs stay of order one
+    wd_scale: float = 1.0
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -88,6 +93,13 @@ PROFILE_WORKLOADS = {
     "prof_fine_grained": Workload("prof_fine_grained", T=2048, d=7168, N=64, F=2048, k=8,
                                   F_sh=2048, score="sigmoid", bias_zipf_s=1.1),
     "prof_switch": Workload("prof_switch", T=16384, d=2048, N=128, F=768, k=1, norm="none"),
+    # the named batches' T, d, N, k, scoring and bias with narrow experts:
+    # h and W_r are drawn first, so the routing, dispatch and combine see the
+    # same data as the full workloads while the device holds a few hundred MB
+    "io_prefill": Workload("io_prefill", T=4096, d=4096, N=8, F=128, k=2),
+    "io_fine_grained": Workload("io_fine_grained", T=8192, d=7168, N=256, F=64, k=8, F_sh=64,
+                                score="sigmoid", bias_zipf_s=1.1),
+    "io_switch": Workload("io_switch", T=65536, d=2048, N=128, F=64, k=1, norm="none"),
 }
 
 
@@ -137,11 +149,11 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", shared: bool = True):
     out["W_r"] = _randn(gen, (w.N, w.d), w.wr_std, dt, dev)
     out["W_gate"] = _randn(gen, (w.N, w.F, w.d), 1.0 / math.sqrt(w.d), dt, dev)
     out["W_up"] = _randn(gen, (w.N, w.F, w.d), 1.0 / math.sqrt(w.d), dt, dev)
-    out["W_down"] = _randn(gen, (w.N, w.d, w.F), 1.0 / math.sqrt(w.F), dt, dev)
+    out["W_down"] = _randn(gen, (w.N, w.d, w.F), w.wd_scale / math.sqrt(w.F), dt, dev)
     if w.F_sh > 0 and shared:
         out["Ws_gate"] = _randn(gen, (w.F_sh, w.d), 1.0 / math.sqrt(w.d), dt, dev)
         out["Ws_up"] = _randn(gen, (w.F_sh, w.d), 1.0 / math.sqrt(w.d), dt, dev)
-        out["Ws_down"] = _randn(gen, (w.d, w.F_sh), 1.0 / math.sqrt(w.F_sh), dt, dev)
+        out["Ws_down"] = _randn(gen, (w.d, w.F_sh), w.wd_scale / math.sqrt(w.F_sh), dt, dev)
     else:
         out["Ws_gate"] = out["Ws_up"] = out["Ws_down"] = None
     if w.bias_zipf_s is not None:
