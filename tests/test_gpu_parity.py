@@ -460,3 +460,50 @@ def test_forward_replays_from_a_cuda_graph(cuda_lib, name):
     ref = run_forward(cfg, inp)
     for k_ in ("out", "idx", "gate"):
         assert torch.equal(outs[k_], ref[k_]), f"{k_}: replay on new inputs differs"
+
+
+def test_expert_ffn_group_sizes_around_tile_boundaries(cuda_lib):
+    """Groups of 0..300 rows through moe_expert_ffn, against the oracle's
+    expert rows. Tiles with at most 96 valid rows run with swapped operands
+    (the weight rows on the tensor core's 128-wide side, the tile's rows as a
+    narrow MMA width loaded in 32-row boxes): the sizes cross the MMA-width
+    steps (16), the box steps (32), the swap limit (96/97) and the full tile
+    (128/129); F = d = 320 leave ragged output tiles on both passes; a shared
+    expert runs beside them as a dense group. The gather-fed variant must give
+    bitwise the same rows."""
+    sizes = [1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 95, 96, 97, 127, 128, 129, 0, 200, 300, 5]
+    N, R, d, F = len(sizes), sum(sizes), 320, 320
+    w = Workload("sizes", T=R, d=d, N=N, F=F, k=1, F_sh=192, wd_scale=0.5)
+    cfg = api.config_for(w)
+    inp = synth.make_inputs(w, seed=12, device="cpu")
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    g = gpu_inputs(inp)
+    off_t = torch.from_numpy(offsets).to(torch.int32).cuda()
+    ws = api.alloc_workspace(cfg, "cuda")
+    y = torch.empty((R, d), dtype=torch.bfloat16, device="cuda")
+    ysh = torch.empty((R, d), dtype=torch.bfloat16, device="cuda")
+    # the rows of h are the dispatched rows themselves (row r belongs to the
+    # group whose offsets bracket r)
+    api.moe_expert_ffn(cfg, g["h"], off_t, g["W_gate"], g["W_up"], g["W_down"], y, g["h"],
+                       g["Ws_gate"], g["Ws_up"], g["Ws_down"], ysh, ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    o = oracle_inputs(inp)
+    ref = O.expert_rows(o["h"], offsets, o["W_gate"], o["W_up"], o["W_down"])
+    for e in range(N):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            assert_close_tol(np_f(y[r0:r1]), ref[r0:r1], BF16_TOL, f"group of {r1 - r0} rows")
+    assert_close_tol(np_f(ysh), O.swiglu_expert(o["h"], o["Ws_gate"], o["Ws_up"], o["Ws_down"]),
+                     BF16_TOL, "shared expert")
+    # gather-fed: row r of the routed operand is h[row_token[r]]; a reversed
+    # permutation makes the gathered rows differ from a plain tile load
+    perm = torch.arange(R - 1, -1, -1, dtype=torch.int32)
+    h_perm = g["h"][perm.long().cuda()].contiguous()          # h_perm[row_token[r]] = h[r]
+    y2 = torch.empty_like(y)
+    ysh2 = torch.empty_like(ysh)
+    api.moe_expert_ffn_gather(cfg, h_perm, perm.cuda(), off_t, g["W_gate"], g["W_up"],
+                              g["W_down"], y2, g["Ws_gate"], g["Ws_up"], g["Ws_down"], ysh2, ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    assert torch.equal(y2, y)

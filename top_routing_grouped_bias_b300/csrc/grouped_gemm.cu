@@ -75,6 +75,11 @@ constexpr size_t kDynSmem = static_cast<size_t>(kStages) * kStageBytes + 1024;
 constexpr uint64_t kWaitBudgetNs = 4000000000ull;   // 4 s per wait
 constexpr int kPairMinRowsPerExpert = MOE_PAIR_MIN_ROWS;
 constexpr uint64_t kDrainBudgetNs = 200000000ull;   // 0.2 s
+// Routed m-tiles with at most this many valid rows run with swapped operands
+// (see the header comment): their rows are loaded as 32-row boxes.
+constexpr int kSwapMaxRows = 96;
+constexpr int kSwapBoxRows = 32;
+constexpr uint32_t kSwapBoxBytes = kSwapBoxRows * 128;
 
 enum { kSwiGLU = 0, kDown = 1, kRoute = 2, kLogits = 3 };
 
@@ -120,7 +125,23 @@ struct GemmParams {
 
 struct TileInfo {
   int g, m_blk, n_blk, row0, rows, ncols, b_row0, num_kb;
+  // swapped tile (0 = no): MMA width N over the tile's valid rows, rounded
+  // up to 16; rv = valid rows of the tile
+  int nr, rv;
 };
+
+// Decides whether a tile of the 1-CTA kernel runs with swapped operands:
+// bf16 gate/up or down passes, routed groups, at most kSwapMaxRows valid
+// rows in the m-tile.
+template <int MODE, typename T>
+__device__ __forceinline__ void set_swap(TileInfo& ti, const GemmParams& p) {
+  ti.rv = min(kBM, ti.rows - ti.m_blk * kBM);
+  ti.nr = 0;
+  if constexpr ((MODE == kSwiGLU || MODE == kDown) && sizeof(T) == 2) {
+    if (ti.g < p.n_routed && ti.rv <= kSwapMaxRows && ti.rv > 0)
+      ti.nr = (ti.rv + 15) / 16 * 16;
+  }
+}
 
 template <int BN, int BK, int BM = kBM>
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int* tile_start, const int* grp_off,
@@ -356,6 +377,53 @@ __device__ __forceinline__ void route_epilogue(uint32_t tbase, int64_t row, bool
   }
 }
 
+// Epilogue of a swapped tile. Accumulator columns [0, nr) hold D0 = W0 X^T
+// and [128, 128 + nr) hold D1 = W1 X^T, with W0/W1 the two 128-row halves of
+// the stage's weight tile and X the tile's rows. Thread `lane_row` owns weight
+// row lane_row of both halves:
+//   gate/up: act[r][col0 + lane_row] = SiLU(D0[lane_row][r]) * D1[lane_row][r]
+//   down:    y[r][col0 + lane_row] = D0, y[r][col0 + 128 + lane_row] = D1
+//            (or gate * y into the token's output row when the combine is fused)
+template <int MODE>
+__device__ __forceinline__ void swap_epilogue(uint32_t tbase, const TileInfo& ti, int lane_row,
+                                              const GemmParams& p) {
+  using bf = __nv_bfloat16;
+  constexpr int BN = MODE == kSwiGLU ? 128 : 256;
+  const int c0 = ti.n_blk * BN + lane_row;
+  const int c1 = c0 + 128;
+  const int r0 = ti.row0 + ti.m_blk * kBM;  // first row of the tile in the routed operand
+#pragma unroll 1
+  for (int c = 0; c < ti.nr; c += 32) {
+    uint32_t d0[32], d1[32];
+    tmem_ld32_sync(tbase + c, d0);
+    tmem_ld32_sync(tbase + kAccCols / 2 + c, d1);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int r = c + j;
+      if (r < ti.rv) {
+        const float v0 = __uint_as_float(d0[j]);
+        const float v1 = __uint_as_float(d1[j]);
+        if (MODE == kSwiGLU) {
+          if (c0 < ti.ncols)
+            static_cast<bf*>(p.out)[static_cast<size_t>(r0 + r) * p.n_out + c0] =
+                __float2bfloat16_rn(v0 / (1.0f + __expf(-v0)) * v1);
+        } else {
+          size_t base = static_cast<size_t>(r0 + r) * p.n_out;
+          float scale = 1.f;
+          if (p.scatter_token != nullptr) {
+            const int tok = p.scatter_token[r0 + r];
+            scale = p.scatter_gate[tok];
+            base = static_cast<size_t>(tok) * p.n_out;
+          }
+          bf* o = static_cast<bf*>(p.out) + base;
+          if (c0 < ti.ncols) o[c0] = __float2bfloat16_rn(v0 * scale);
+          if (c1 < ti.ncols) o[c1] = __float2bfloat16_rn(v1 * scale);
+        }
+      }
+    }
+  }
+}
+
 template <int MODE, typename T, int KT = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA0,
@@ -363,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mapB0u,
                         const __grid_constant__ CUtensorMap mapA1,
                         const __grid_constant__ CUtensorMap mapB1,
-                        const __grid_constant__ CUtensorMap mapB1u, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap mapB1u,
+                        const __grid_constant__ CUtensorMap mapAs, const GemmParams p) {
   constexpr int BK = 128 / static_cast<int>(sizeof(T));   // elements per 128-byte row
   constexpr int BN = MODE == kSwiGLU ? 128 : 256;         // output columns per tile
   // kRoute / kLogits: one accumulator of n_out = N rounded up to 16 columns
@@ -463,10 +532,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       int split = 0, kb0 = 0;
-      const TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
-                                          : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+      TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
+                                    : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+      set_swap<MODE, T>(ti, p);
       const bool dense = ti.g >= p.n_routed;
       const bool gather = MODE == kSwiGLU && p.gather_rows != nullptr && !dense;
+      const int nbox = ti.nr > 0 ? (ti.rv + kSwapBoxRows - 1) / kSwapBoxRows : 0;
+      const uint32_t tile_tx = ti.nr > 0 ? kStageB + static_cast<uint32_t>(nbox) * kSwapBoxBytes
+                                         : stage_tx;
       const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
       const void* mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
       const void* mBu = dense ? static_cast<const void*>(&mapB1u) : static_cast<const void*>(&mapB0u);
@@ -486,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           w = mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_v, p.status, p.budget_ns,
                                 MOE_ERR_TIMEOUT);
-          if (w) mbar_arrive_expect_tx(&full_bar[stage], stage_tx);
+          if (w) mbar_arrive_expect_tx(&full_bar[stage], tile_tx);
         }
         w = __shfl_sync(0xffffffffu, w, 0);
         if (!w) {
@@ -495,9 +568,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* sA = smem + stage * kStageBytes;
         uint8_t* sB = sA + kStageA;
-        if (gather) tma_gather4(sA + lane * 512, mA, &full_bar[stage], (kb0 + kb) * BK, g4[0], g4[1], g4[2], g4[3]);
+        // gathered rows: one gather4 (4 rows) per lane, over the 32-row boxes
+        // of a swapped tile or the whole 128-row tile
+        if (gather && (ti.nr == 0 || lane < nbox * (kSwapBoxRows / 4)))
+          tma_gather4(sA + lane * 512, mA, &full_bar[stage], (kb0 + kb) * BK, g4[0], g4[1], g4[2],
+                      g4[3]);
         if (lane == 0) {
-          if (!gather) tma_load_2d(sA, mA, &full_bar[stage], (kb0 + kb) * BK, a_row);
+          if (ti.nr > 0 && !gather) {
+            // the tile's valid rows as 32-row boxes, stacked like one taller box
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d(sA + b * kSwapBoxBytes, &mapAs, &full_bar[stage], (kb0 + kb) * BK,
+                          a_row + b * kSwapBoxRows);
+          } else if (!gather) {
+            tma_load_2d(sA, mA, &full_bar[stage], (kb0 + kb) * BK, a_row);
+          }
           if (MODE == kSwiGLU) {
             tma_load_2d(sB, mB, &full_bar[stage], (kb0 + kb) * BK, b_row);
             tma_load_2d(sB + kStageB / 2, mBu, &full_bar[stage], (kb0 + kb) * BK, b_row);
@@ -525,8 +609,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         int split = 0, kb0 = 0;
-        const TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
-                                            : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+        TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
+                                      : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+        set_swap<MODE, T>(ti, p);
+        const uint32_t idesc_swap = make_idesc(kBM, ti.nr > 0 ? ti.nr : 16, 1u);
         if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, abort_v, p.status, p.budget_ns,
                                MOE_ERR_TIMEOUT)) {
           ok = false;
@@ -543,15 +629,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
           const uint32_t b_addr = a_addr + kStageA;
+          if (ti.nr > 0) {
+            // swapped: the two 128-row weight halves of the B stage are the
+            // A operands, the tile's rows the (narrow) B operand
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sw128_kmajor_desc(a_addr + kk * 32);
-            const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
-            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
-            if (sizeof(T) == 2)
-              mma_f16(d_tmem, ad, bd, idesc, accum);
-            else
-              mma_tf32(d_tmem, ad, bd, idesc, accum);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t xd = sw128_kmajor_desc(a_addr + kk * 32);
+              const uint64_t w0 = sw128_kmajor_desc(b_addr + kk * 32);
+              const uint64_t w1 = sw128_kmajor_desc(b_addr + kStageB / 2 + kk * 32);
+              const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+              mma_f16(d_tmem, w0, xd, idesc_swap, accum);
+              mma_f16(d_tmem + kAccCols / 2, w1, xd, idesc_swap, accum);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sw128_kmajor_desc(a_addr + kk * 32);
+              const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
+              const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+              if (sizeof(T) == 2)
+                mma_f16(d_tmem, ad, bd, idesc, accum);
+              else
+                mma_tf32(d_tmem, ad, bd, idesc, accum);
+            }
           }
           mma_commit(&empty_bar[stage]);
           if (++stage == kStages) {
@@ -579,8 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int split = 0, kb0 = 0;
-      const TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
-                                          : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+      TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
+                                    : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+      set_swap<MODE, T>(ti, p);
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_v, p.status, p.budget_ns,
                              MOE_ERR_TIMEOUT))
         break;
@@ -601,7 +702,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         out = static_cast<T*>(p.out) + static_cast<size_t>(tok) * p.n_out;
       }
       out += col0;
-      if (MODE == kRoute) {
+      if (ti.nr > 0) {
+        // swapped tile: this thread's TMEM lane is one output column (a row
+        // of the weight tile), its TMEM columns are the tile's rows
+        swap_epilogue<MODE>(tbase, ti, row_in_tile, p);
+      } else if (MODE == kRoute) {
         route_epilogue<KT>(tbase, row, row_ok, p.n_out, p.re);
       } else if (MODE == kLogits) {
         // this unit's partial logits, rows of the tile x n_out columns
@@ -1013,7 +1118,8 @@ cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid, 
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kDynSmem));
   if (err != cudaSuccess) return err;
-  kern<<<grid, kThreads, kDynSmem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  kern<<<grid, kThreads, kDynSmem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                                              maps[6], p);
   return cudaGetLastError();
 }
 
@@ -1089,14 +1195,17 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   const int64_t R = a.rows > 0 ? a.rows : a.T * a.k;
   const bool sh = a.F_sh > 0;
   const int sms = num_sms();
-  CUtensorMap m[6];
+  CUtensorMap m[7];
 
   // pass A: act = SiLU(x Wg^T) * (x Wu^T); x is the dispatched copy, or the
-  // rows of h picked by index (gather4, 1-row box) when gather_rows is given
+  // rows of h picked by index (gather4, 1-row box) when gather_rows is given.
+  // m[6]: x in 32-row boxes for the swapped tiles (not used when gathering)
   const bool gather = a.gather_rows != nullptr;
   if (gather) {
     if (!make_map(&m[0], a.h, a.dtype, a.d, a.T, 1)) return cudaErrorInvalidValue;
-  } else if (!make_map(&m[0], a.x_disp, a.dtype, a.d, R, kBM)) {
+    m[6] = m[0];
+  } else if (!make_map(&m[0], a.x_disp, a.dtype, a.d, R, kBM) ||
+             !make_map(&m[6], a.x_disp, a.dtype, a.d, R, kSwapBoxRows)) {
     return cudaErrorInvalidValue;
   }
   if (!make_map(&m[1], a.W_gate, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, 128)) return cudaErrorInvalidValue;
@@ -1138,7 +1247,9 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
 
   // pass B: y = act Wd^T
-  if (!make_map(&m[0], a.act, a.dtype, a.F, R, kBM)) return cudaErrorInvalidValue;
+  if (!make_map(&m[0], a.act, a.dtype, a.F, R, kBM) ||
+      !make_map(&m[6], a.act, a.dtype, a.F, R, kSwapBoxRows))
+    return cudaErrorInvalidValue;
   // a CTA pair splits the 256 B rows of a down tile 128/128 between its CTAs
   const uint32_t down_box = pair ? 128 : 256;
   if (!make_map(&m[1], a.W_down, a.dtype, a.F, static_cast<uint64_t>(a.N) * a.d, down_box))
@@ -1175,11 +1286,11 @@ bool route_on_tensor_cores(const RouteArgs& a) {
 
 cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t stream) {
   const RouteSplit rs = route_split(a.T, a.d, a.N);
-  CUtensorMap m[6];
+  CUtensorMap m[7];
   if (!make_map(&m[0], a.h, a.dtype, a.d, a.T, kBM)) return cudaErrorInvalidValue;
   if (!make_map(&m[1], a.W_r, a.dtype, a.d, a.N, static_cast<uint32_t>(rs.n_pad)))
     return cudaErrorInvalidValue;
-  m[2] = m[1]; m[3] = m[0]; m[4] = m[1]; m[5] = m[1];
+  m[2] = m[1]; m[3] = m[0]; m[4] = m[1]; m[5] = m[1]; m[6] = m[0];
   GemmParams p{};
   p.offsets = nullptr;
   p.n_routed = 1;
@@ -1201,11 +1312,11 @@ cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_route_mma(const RouteArgs& a, cudaStream_t stream) {
   const int n_pad = (a.N + 15) / 16 * 16;
-  CUtensorMap m[6];
+  CUtensorMap m[7];
   if (!make_map(&m[0], a.h, a.dtype, a.d, a.T, kBM)) return cudaErrorInvalidValue;
   if (!make_map(&m[1], a.W_r, a.dtype, a.d, a.N, static_cast<uint32_t>(n_pad)))
     return cudaErrorInvalidValue;
-  m[2] = m[1]; m[3] = m[0]; m[4] = m[1]; m[5] = m[1];
+  m[2] = m[1]; m[3] = m[0]; m[4] = m[1]; m[5] = m[1]; m[6] = m[0];
   GemmParams p{};
   p.offsets = nullptr;
   p.n_routed = 1;
