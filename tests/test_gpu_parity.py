@@ -464,8 +464,8 @@ def test_forward_replays_from_a_cuda_graph(cuda_lib, name):
 
 def test_expert_ffn_group_sizes_around_tile_boundaries(cuda_lib):
     """Groups of 0..300 rows through moe_expert_ffn, against the oracle's
-    expert rows. Tiles with at most 96 valid rows run with swapped operands
-    (the weight rows on the tensor core's 128-wide side, the tile's rows as a
+    expert rows. Groups of at most 96 rows run with swapped operands (the
+    weight rows on the tensor core's 128-wide side, the group's rows as a
     narrow MMA width loaded in 32-row boxes): the sizes cross the MMA-width
     steps (16), the box steps (32), the swap limit (96/97) and the full tile
     (128/129); F = d = 320 leave ragged output tiles on both passes; a shared
@@ -504,6 +504,54 @@ def test_expert_ffn_group_sizes_around_tile_boundaries(cuda_lib):
     ysh2 = torch.empty_like(ysh)
     api.moe_expert_ffn_gather(cfg, h_perm, perm.cuda(), off_t, g["W_gate"], g["W_up"],
                               g["W_down"], y2, g["Ws_gate"], g["Ws_up"], g["Ws_down"], ysh2, ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    assert torch.equal(y2, y)
+
+
+def test_pair_kernel_tails_around_swap_boundaries(cuda_lib):
+    """Groups large enough for the CTA-pair kernel (>= 768 rows per expert on
+    average), whose last 256-row tiles hold 1..250 rows: tails of at most 64
+    rows run with swapped operands (weights on the M=256 side, the tail rows
+    as N split over the pair), the others as plain tiles. One group is a
+    64-row tail alone, one is empty. F = 384 and d = 320 leave ragged output
+    tiles; a shared expert runs as a dense group. Checked against the
+    oracle's expert rows; the gather-fed variant must give bitwise the same
+    rows."""
+    sizes = [1025, 1040, 1041, 1057, 1087, 64, 1088, 1089, 1274, 0, 1040, 17]
+    N, R, d, F = len(sizes), sum(sizes), 320, 384
+    assert R >= 768 * N, "the grouped GEMM must run on CTA pairs"
+    w = Workload("pair_tails", T=R, d=d, N=N, F=F, k=1, F_sh=128, wd_scale=0.5)
+    cfg = api.config_for(w)
+    inp = synth.make_inputs(w, seed=13, device="cpu")
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    g = gpu_inputs(inp)
+    off_t = torch.from_numpy(offsets).to(torch.int32).cuda()
+    ws = api.alloc_workspace(cfg, "cuda")
+    y = torch.empty((R, d), dtype=torch.bfloat16, device="cuda")
+    ysh = torch.empty((R, d), dtype=torch.bfloat16, device="cuda")
+    api.moe_expert_ffn(cfg, g["h"], off_t, g["W_gate"], g["W_up"], g["W_down"], y, g["h"],
+                       g["Ws_gate"], g["Ws_up"], g["Ws_down"], ysh, ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    o = oracle_inputs(inp)
+    for e in range(N):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            # the last 256-row tile (swapped or plain) and the rows before it
+            lo = max(r0, r0 + (r1 - r0) // 256 * 256 - 40)
+            ref = O.swiglu_expert(o["h"][lo:r1], o["W_gate"][e], o["W_up"][e], o["W_down"][e])
+            assert_close_tol(np_f(y[lo:r1]), ref, BF16_TOL, f"group of {r1 - r0} rows")
+    toks = np.arange(0, R, 37)
+    assert_close_tol(np_f(ysh[torch.from_numpy(toks).cuda()]),
+                     O.swiglu_expert(o["h"][toks], o["Ws_gate"], o["Ws_up"], o["Ws_down"]),
+                     BF16_TOL, "shared expert")
+    perm = torch.arange(R - 1, -1, -1, dtype=torch.int32)
+    h_perm = g["h"][perm.long().cuda()].contiguous()
+    y2 = torch.empty_like(y)
+    api.moe_expert_ffn_gather(cfg, h_perm, perm.cuda(), off_t, g["W_gate"], g["W_up"],
+                              g["W_down"], y2, g["Ws_gate"], g["Ws_up"], g["Ws_down"],
+                              torch.empty_like(ysh), ws)
     torch.cuda.synchronize()
     assert api.read_status(ws) == api.MOE_OK
     assert torch.equal(y2, y)

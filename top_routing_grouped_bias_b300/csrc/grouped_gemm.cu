@@ -22,6 +22,16 @@
 // W_up, so one N=256 MMA produces the gate half (columns 0..127) and the up
 // half (128..255) of a 128-column output tile.
 //
+// Light experts (groups of at most 96 rows) run their tiles with swapped
+// operands: the same shared-memory stage, but the two 128-row weight halves
+// (W_gate / W_up, or the two halves of the 256-row W_down tile) are the A
+// operands of two M=128 MMAs and the group's rows are the B operand with N =
+// rows rounded up to 16, loaded as 32-row boxes. Accumulator columns [0, N)
+// and [128, 128 + N) hold the two products, transposed (TMEM lane = output
+// column); the epilogue writes them back row by row. Such tiles stream their
+// weights from HBM for few rows; the swap keeps them from also issuing a
+// zero-padded 128 x 256 MMA per K-step.
+//
 // Two more instances are the router: logits = h W_r^T for 128 tokens per tile
 // with all N <= 256 experts in one accumulator.
 //   kRoute   (batches of at least ~148 token tiles) does the whole routing in
@@ -75,11 +85,19 @@ constexpr size_t kDynSmem = static_cast<size_t>(kStages) * kStageBytes + 1024;
 constexpr uint64_t kWaitBudgetNs = 4000000000ull;   // 4 s per wait
 constexpr int kPairMinRowsPerExpert = MOE_PAIR_MIN_ROWS;
 constexpr uint64_t kDrainBudgetNs = 200000000ull;   // 0.2 s
-// Routed m-tiles with at most this many valid rows run with swapped operands
-// (see the header comment): their rows are loaded as 32-row boxes.
-constexpr int kSwapMaxRows = 96;
+// Groups of at most this many rows run with swapped operands (see the
+// header comment): their rows are loaded as 32-row boxes.
+#ifndef MOE_SWAP_MAX_ROWS
+#define MOE_SWAP_MAX_ROWS 96
+#endif
+constexpr int kSwapMaxRows = MOE_SWAP_MAX_ROWS;
 constexpr int kSwapBoxRows = 32;
 constexpr uint32_t kSwapBoxBytes = kSwapBoxRows * 128;
+// CTA-pair kernel: last tiles of at most this many rows run swapped.
+#ifndef MOE_PAIR_SWAP_ROWS
+#define MOE_PAIR_SWAP_ROWS 64
+#endif
+constexpr int kPairSwapRows = MOE_PAIR_SWAP_ROWS;
 
 enum { kSwiGLU = 0, kDown = 1, kRoute = 2, kLogits = 3 };
 
@@ -131,14 +149,23 @@ struct TileInfo {
 };
 
 // Decides whether a tile of the 1-CTA kernel runs with swapped operands:
-// bf16 gate/up or down passes, routed groups, at most kSwapMaxRows valid
-// rows in the m-tile.
+// bf16 gate/up or down passes, routed groups of at most kSwapMaxRows rows in
+// all (light experts, whose tiles stream weights for few rows). The tails of
+// larger groups keep the plain tile: measured, their swapped form (more TMA
+// loads per stage, scalar epilogue stores) was slower.
+// Whether routed group g of the pair kernel runs its last tile, of `tail`
+// rows, with swapped operands (see the pair kernel's header comment).
+template <int MODE>
+__device__ __forceinline__ bool pair_swap_tail(int g, int tail, const GemmParams& p) {
+  return (MODE == kSwiGLU || MODE == kDown) && g < p.n_routed && tail > 0 && tail <= kPairSwapRows;
+}
+
 template <int MODE, typename T>
 __device__ __forceinline__ void set_swap(TileInfo& ti, const GemmParams& p) {
   ti.rv = min(kBM, ti.rows - ti.m_blk * kBM);
   ti.nr = 0;
   if constexpr ((MODE == kSwiGLU || MODE == kDown) && sizeof(T) == 2) {
-    if (ti.g < p.n_routed && ti.rv <= kSwapMaxRows && ti.rv > 0)
+    if (ti.g < p.n_routed && ti.rows <= kSwapMaxRows && ti.rv > 0)
       ti.nr = (ti.rv + 15) / 16 * 16;
   }
 }
@@ -780,11 +807,123 @@ __global__ void __launch_bounds__(kThreads, 1)
 // full barrier, the leader's commits arrive on both CTAs' empty and
 // accumulator-full barriers, and both CTAs' epilogue threads arrive on the
 // leader's accumulator-empty barrier. Each CTA drains its own 128 TMEM lanes.
+//
+// Short tails. A routed group whose last 256-row tile holds at most
+// kPairSwapRows rows runs that tile with swapped operands: the weights are
+// the M=256 side of the pair MMA (128 weight rows per CTA) and the tail rows
+// the B operand, N = tail rounded up to 16, split N/2 per CTA (one 32-row box
+// in a third 4 KB region of the stage). Pass A: CTA r holds W_gate rows
+// f0 + 128 r + [0,128) in the A region and the same W_up rows in the B region;
+// two MMAs give gate and up of those columns for every tail row in the
+// accumulator's columns [0, N) and [128, 128 + N), so one swapped tile covers
+// 256 output columns (a plain pass-A tile covers 128). Pass B: CTA r holds
+// W_down rows c0 + 128 r + [0,128); one MMA covers the tile's 256 output
+// columns. TMEM lane = output column; the epilogue writes back row by row.
+// A tail of 4..64 rows no longer costs a 256 x 256 MMA per K-step.
 constexpr int kPairStages = MOE_PAIR_STAGES;
 constexpr uint32_t kPairStageA = 128 * 128;
 constexpr uint32_t kPairStageB = 128 * 128;
-constexpr uint32_t kPairStageBytes = kPairStageA + kPairStageB;
+constexpr uint32_t kPairStageX = kSwapBoxBytes;   // tail rows of a swapped tile
+constexpr uint32_t kPairStageBytes = kPairStageA + kPairStageB + kPairStageX;
 constexpr size_t kPairDynSmem = static_cast<size_t>(kPairStages) * kPairStageBytes + 1024;
+static_assert(kPairSwapRows <= 2 * kSwapBoxRows, "a CTA's half of a swapped tail fits one box");
+
+// Epilogue of a swapped tail of the pair kernel. Accumulator columns [0, N)
+// hold W0 X^T and (pass A) [128, 128 + N) hold W1 X^T, with W0 / W1 this
+// CTA's 128 rows of W_gate / W_up (pass A) or of W_down (pass B) and X the
+// tile's rows; thread `lane_row` owns output column
+// o = 256 n_blk + 128 rank + lane_row:
+//   gate/up: act[r][o] = SiLU(W_gate X^T) * (W_up X^T)
+//   down:    y[r][o] = W_down X^T (or gate * y into the token's row when the
+//            combine is fused)
+template <int MODE>
+__device__ __forceinline__ void pair_swap_epilogue(uint32_t tbase, const TileInfo& ti,
+                                                   int lane_row, int rank,
+                                                   const GemmParams& p) {
+  using bf = __nv_bfloat16;
+  const int o = ti.n_blk * 256 + rank * 128 + lane_row;
+  const int r0 = ti.row0 + ti.m_blk * 256;
+#pragma unroll 1
+  for (int c = 0; c < ti.nr; c += 32) {
+    uint32_t d0[32], d1[32];
+    tmem_ld32_sync(tbase + c, d0);
+    if (MODE == kSwiGLU) tmem_ld32_sync(tbase + kAccCols / 2 + c, d1);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int r = c + j;
+      if (r < ti.rv && o < ti.ncols) {
+        const float v0 = __uint_as_float(d0[j]);
+        if (MODE == kSwiGLU) {
+          const float v1 = __uint_as_float(d1[j]);
+          static_cast<bf*>(p.out)[static_cast<size_t>(r0 + r) * p.n_out + o] =
+              __float2bfloat16_rn(v0 / (1.0f + __expf(-v0)) * v1);
+        } else {
+          size_t base = static_cast<size_t>(r0 + r) * p.n_out;
+          float scale = 1.f;
+          if (p.scatter_token != nullptr) {
+            const int tok = p.scatter_token[r0 + r];
+            scale = p.scatter_gate[tok];
+            base = static_cast<size_t>(tok) * p.n_out;
+          }
+          static_cast<bf*>(p.out)[base + o] = __float2bfloat16_rn(v0 * scale);
+        }
+      }
+    }
+  }
+}
+
+// Tile `tile` of the pair kernel: the band-ordered plain tiles of each group,
+// then (for a swapped tail) its n-tiles of the swapped form. ti.nr = MMA N of
+// a swapped tail (0 for a plain tile), ti.rv = valid rows of the tile.
+template <int MODE, int BN, int BK>
+__device__ __forceinline__ TileInfo decode_pair_tile(int tile, const int* tile_start,
+                                                     const int* grp_off, int G,
+                                                     const GemmParams& p) {
+  constexpr int BM = 256;
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_start[mid] <= tile) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  ti.g = lo;
+  if (lo < p.n_routed) {
+    ti.row0 = grp_off[lo];
+    ti.rows = grp_off[lo + 1] - grp_off[lo];
+    ti.ncols = p.n_out;
+    ti.b_row0 = lo * p.n_out;
+    ti.num_kb = (p.K + BK - 1) / BK;
+  } else {
+    ti.row0 = 0;
+    ti.rows = p.rows_shared;
+    ti.ncols = p.n_out_shared;
+    ti.b_row0 = 0;
+    ti.num_kb = (p.K_shared + BK - 1) / BK;
+  }
+  const int tail = ti.rows % BM;
+  const bool swap = pair_swap_tail<MODE>(lo, tail, p);
+  const int mt = ti.rows / BM + (tail > 0 && !swap ? 1 : 0);  // plain m-tiles
+  const int nt = (ti.ncols + BN - 1) / BN;
+  const int l = tile - tile_start[lo];
+  ti.nr = 0;
+  if (l >= mt * nt) {
+    // swapped tail: n-tiles of 256 output columns (pass A) or BN (pass B)
+    ti.m_blk = ti.rows / BM;
+    ti.n_blk = l - mt * nt;
+    ti.rv = tail;
+    ti.nr = (tail + 15) / 16 * 16;
+    return ti;
+  }
+  const int nbands0 = (mt + kBandMax * kBM / BM - 1) / (kBandMax * kBM / BM);
+  const int band_sz = (mt + nbands0 - 1) / nbands0;
+  const int band = l / (band_sz * nt);
+  const int r = l - band * band_sz * nt;
+  const int bs = min(band_sz, mt - band * band_sz);
+  ti.n_blk = r / bs;
+  ti.m_blk = band * band_sz + (r - ti.n_blk * bs);
+  ti.rv = min(BM, ti.rows - ti.m_blk * BM);
+  return ti;
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -793,7 +932,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap mapB0u,
                              const __grid_constant__ CUtensorMap mapA1,
                              const __grid_constant__ CUtensorMap mapB1,
-                             const __grid_constant__ CUtensorMap mapB1u, const GemmParams p) {
+                             const __grid_constant__ CUtensorMap mapB1u,
+                             const __grid_constant__ CUtensorMap mapAs, const GemmParams p) {
   using T = __nv_bfloat16;
   constexpr int BK = 64;
   constexpr int BM = 256;                                  // rows per pair tile
@@ -857,7 +997,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (g < G) {
         const int rows = g < p.n_routed ? grp_off[g + 1] - grp_off[g] : p.rows_shared;
         const int ncols = g < p.n_routed ? p.n_out : p.n_out_shared;
-        tiles = ((rows + BM - 1) / BM) * ((ncols + BN - 1) / BN);
+        const int nt = (ncols + BN - 1) / BN;
+        if (pair_swap_tail<MODE>(g, rows % BM, p))
+          tiles = (rows / BM) * nt + (MODE == kSwiGLU ? (ncols + 255) / 256 : nt);
+        else
+          tiles = ((rows + BM - 1) / BM) * nt;
       }
       int incl = tiles;
 #pragma unroll
@@ -884,9 +1028,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
-      const TileInfo ti = decode_tile<BN, BK, BM>(tile, tile_start, grp_off, G, p);
+      const TileInfo ti = decode_pair_tile<MODE, BN, BK>(tile, tile_start, grp_off, G, p);
       const bool dense = ti.g >= p.n_routed;
       const bool gather = MODE == kSwiGLU && p.gather_rows != nullptr && !dense;
+      const bool swapped = ti.nr > 0;
+      // bytes per stage of both CTAs: plain tiles A + B; swapped tails the
+      // weight rows (both halves in pass A, one in pass B) and the tail box
+      const uint32_t tile_tx =
+          swapped ? 2 * ((MODE == kSwiGLU ? kPairStageA + kPairStageB : kPairStageA) + kPairStageX)
+                  : 2 * (kPairStageA + kPairStageB);
       const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
       const void* mB;
       int b_row;
@@ -899,7 +1049,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
         b_row = ti.b_row0 + ti.n_blk * BN + static_cast<int>(rank) * 128;
       }
-      const int a_row = ti.row0 + ti.m_blk * BM + static_cast<int>(rank) * 128;
+      // a swapped tail: CTA r holds tail rows [r N/2, r N/2 + 32) and weight
+      // rows 128 r + [0,128) of the tile's 256 output columns
+      const int a_row = swapped ? ti.row0 + ti.m_blk * BM + static_cast<int>(rank) * (ti.nr / 2)
+                                : ti.row0 + ti.m_blk * BM + static_cast<int>(rank) * 128;
+      const int w_row = ti.b_row0 + ti.n_blk * 256 + static_cast<int>(rank) * 128;
       int g4[4] = {0, 0, 0, 0};
       if (gather) {
 #pragma unroll
@@ -920,14 +1074,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* sA = smem + stage * kPairStageBytes;
         uint8_t* sB = sA + kPairStageA;
+        uint8_t* sX = sB + kPairStageB;
         const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[stage]), 0);
-        if (lane == 0 && leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
+        if (lane == 0 && leader) mbar_arrive_expect_tx(&full_bar[stage], tile_tx);
         __syncwarp();
-        if (gather)
-          tma_gather4_pair(sA + lane * 512, mA, full_leader, kb * BK, g4[0], g4[1], g4[2], g4[3]);
-        if (lane == 0) {
-          if (!gather) tma_load_2d_pair(sA, mA, full_leader, kb * BK, a_row);
-          tma_load_2d_pair(sB, mB, full_leader, kb * BK, b_row);
+        if (swapped) {
+          // tail rows into the X region (a 32-row box, or 8 gather4 lanes)
+          if (gather) {
+            if (lane < kSwapBoxRows / 4)
+              tma_gather4_pair(sX + lane * 512, mA, full_leader, kb * BK, g4[0], g4[1], g4[2],
+                               g4[3]);
+          } else if (lane == 0) {
+            tma_load_2d_pair(sX, &mapAs, full_leader, kb * BK, a_row);
+          }
+          if (lane == 0) {
+            if (MODE == kSwiGLU) {
+              tma_load_2d_pair(sA, &mapB0, full_leader, kb * BK, w_row);    // W_gate rows
+              tma_load_2d_pair(sB, &mapB0u, full_leader, kb * BK, w_row);   // W_up rows
+            } else {
+              tma_load_2d_pair(sA, &mapB0, full_leader, kb * BK, w_row);    // W_down rows
+            }
+          }
+        } else {
+          if (gather)
+            tma_gather4_pair(sA + lane * 512, mA, full_leader, kb * BK, g4[0], g4[1], g4[2], g4[3]);
+          if (lane == 0) {
+            if (!gather) tma_load_2d_pair(sA, mA, full_leader, kb * BK, a_row);
+            tma_load_2d_pair(sB, mB, full_leader, kb * BK, b_row);
+          }
         }
         if (++stage == kPairStages) {
           stage = 0;
@@ -948,7 +1122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
-        const TileInfo ti = decode_tile<BN, BK, BM>(tile, tile_start, grp_off, G, p);
+        const TileInfo ti = decode_pair_tile<MODE, BN, BK>(tile, tile_start, grp_off, G, p);
+        const uint32_t idesc_swap = make_idesc(BM, ti.nr > 0 ? ti.nr : 16, 1u);
         if (!mbar_wait_bounded_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort_v, p.status,
                                        p.budget_ns, MOE_ERR_TIMEOUT)) {
           ok = false;
@@ -965,11 +1140,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + stage * kPairStageBytes);
           const uint32_t b_addr = a_addr + kPairStageA;
+          if (ti.nr > 0) {
+            // swapped tail: weights (A region; W_up in the B region) x tail rows
+            const uint32_t x_addr = b_addr + kPairStageB;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sw128_kmajor_desc(a_addr + kk * 32);
-            const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
-            mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t xd = sw128_kmajor_desc(x_addr + kk * 32);
+              const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+              mma_f16_pair(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), xd, idesc_swap, accum);
+              if (MODE == kSwiGLU)
+                mma_f16_pair(d_tmem + kAccCols / 2, sw128_kmajor_desc(b_addr + kk * 32), xd,
+                             idesc_swap, accum);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sw128_kmajor_desc(a_addr + kk * 32);
+              const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
+              mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           mma_commit_pair(&empty_bar[stage], 0x3);
           if (++stage == kPairStages) {
@@ -998,7 +1187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = cluster_id; tile < total; tile += n_clusters) {
-      const TileInfo ti = decode_tile<BN, BK, BM>(tile, tile_start, grp_off, G, p);
+      const TileInfo ti = decode_pair_tile<MODE, BN, BK>(tile, tile_start, grp_off, G, p);
       if (!mbar_wait_bounded_cluster(&tfull_bar[acc], acc_phase, abort_v, p.status, p.budget_ns,
                                      MOE_ERR_TIMEOUT))
         break;
@@ -1019,7 +1208,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         out = static_cast<T*>(p.out) + static_cast<size_t>(tok) * p.n_out;
       }
       out += col0;
-      if (MODE == kSwiGLU) {
+      if (ti.nr > 0) {
+        // swapped tail: TMEM lane = output column 256 n + 128 rank + lane_row
+        pair_swap_epilogue<MODE>(tbase, ti, row_in_tile, static_cast<int>(rank), p);
+      } else if (MODE == kSwiGLU) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           uint32_t gr[32], ur[32];
@@ -1169,7 +1361,8 @@ cudaError_t launch_gemm_pair(const CUtensorMap* maps, const GemmParams& p, int p
   if (clusters > pair_tiles) clusters = pair_tiles;
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  err = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  err = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                           maps[6], p);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
