@@ -7,10 +7,9 @@
 //
 //   out[t] = y_shared[t] + sum_{j<k} gate[t,j] * y_rows[inv[t*k+j]]
 //
-// A block takes one token at a time (blocks stride over the tokens) and reads
-// its k rows and gates once; its threads stride over the row's 16-byte
-// vectors. fp32 accumulation in slot order (deterministic), rounded once to
-// the output dtype.
+// A warp takes one token at a time and reads its k rows and gates once; its
+// lanes stride over the row's 16-byte vectors. fp32 accumulation in slot
+// order (deterministic), rounded once to the output dtype.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -43,45 +42,72 @@ __device__ __forceinline__ uint4 pack(const float (&f)[4], float*) {
                     __float_as_uint(f[3]));
 }
 
+// A warp per token (warps stride over the tokens): lanes < k fetch the
+// token's rows and gates once and share them by shuffles; the warp then walks
+// the row's 16-byte vectors 32 * U at a time (lane l takes v0 + l + 32 u), so
+// that U loads per slot and lane are in flight, accumulating in slot order.
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   constexpr int V = 16 / sizeof(T);
+  constexpr int U = 4;
   const int nvec = a.d / V;
   const uint4* Y = static_cast<const uint4*>(a.y_rows);
   const uint4* S = static_cast<const uint4*>(a.y_shared);
   uint4* O = static_cast<uint4*>(a.out);
   const int64_t R = a.T * a.k;
-  // the token's rows (first vector, -1 = none) and gates in slot order; only
-  // rows moe_dispatch wrote are read
-  __shared__ int64_t rows[kMaxTopK];
-  __shared__ float g[kMaxTopK];
-  for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-    __syncthreads();  // the previous token's rows are no longer read
-    if (threadIdx.x < a.k) {
-      const int64_t r = a.inv[t * a.k + threadIdx.x];
-      const bool ok = r >= 0 && r < R;
-      rows[threadIdx.x] = ok ? r * nvec : -1;
-      g[threadIdx.x] = ok ? a.gate[t * a.k + threadIdx.x] : 0.f;
-    }
-    __syncthreads();
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-      float acc[V];
-      if (S != nullptr) {
-        unpack(S[t * nvec + v], acc, static_cast<T*>(nullptr));
-      } else {
-#pragma unroll
-        for (int q = 0; q < V; ++q) acc[q] = 0.f;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < a.T; t += warps) {
+    // slot `lane`: first vector of its row (-1 = none; only rows moe_dispatch
+    // wrote are read) and its gate
+    int64_t my_row = -1;
+    float my_g = 0.f;
+    if (lane < a.k) {
+      const int64_t r = a.inv[t * a.k + lane];
+      if (r >= 0 && r < R) {
+        my_row = r * nvec;
+        my_g = a.gate[t * a.k + lane];
       }
-#pragma unroll 4
-      for (int j = 0; j < a.k; ++j) {
-        if (rows[j] >= 0) {
-          float y[V];
-          unpack(Y[rows[j] + v], y, static_cast<T*>(nullptr));
+    }
+    // the same trip count on every lane: the shuffles below need the whole warp
+    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+      float acc[U][V];
 #pragma unroll
-          for (int q = 0; q < V; ++q) acc[q] = fmaf(g[j], y[q], acc[q]);
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (S != nullptr && v < nvec) {
+          unpack(S[t * nvec + v], acc[u], static_cast<T*>(nullptr));
+        } else {
+#pragma unroll
+          for (int q = 0; q < V; ++q) acc[u][q] = 0.f;
         }
       }
-      O[t * nvec + v] = pack(acc, static_cast<T*>(nullptr));
+      for (int j = 0; j < a.k; ++j) {
+        const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
+        const float g = __shfl_sync(0xffffffffu, my_g, j);
+        if (row < 0) continue;
+        uint4 y[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + lane + 32 * u;
+          if (v < nvec) y[u] = Y[row + v];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (v0 + lane + 32 * u < nvec) {
+            float f[V];
+            unpack(y[u], f, static_cast<T*>(nullptr));
+#pragma unroll
+            for (int q = 0; q < V; ++q) acc[u][q] = fmaf(g, f[q], acc[u][q]);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (v < nvec) O[t * nvec + v] = pack(acc[u], static_cast<T*>(nullptr));
+      }
     }
   }
 }
@@ -90,8 +116,10 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
+  // 8 warps (tokens) per block, up to 8 blocks per SM
+  const int64_t need = (a.T + 7) / 8;
   const int64_t blocks = static_cast<int64_t>(num_sms()) * 8;
-  const unsigned grid = static_cast<unsigned>(a.T < blocks ? a.T : blocks);
+  const unsigned grid = static_cast<unsigned>(need < blocks ? need : blocks);
   if (a.dtype == MOE_F32)
     combine_kernel<float><<<grid, 256, 0, stream>>>(a);
   else

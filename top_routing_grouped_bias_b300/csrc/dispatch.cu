@@ -3,8 +3,9 @@
 // Pages: "MOE 专家选择与路由机制" §三 Token Dispatch (pairs of one expert are
 // listed together, tokens ascending); "【大模型】MoE（专家混合模型）简介" §3 ②.
 //
-// Deterministic counting sort in three launches plus the gather, no atomics on
-// the ordering:
+// Deterministic counting sort in three launches plus the gather (one launch
+// plus the gather for small batches: dispatch_small_kernel below), no atomics
+// on the ordering:
 //   1. count    per block of 256 tokens, per-expert pair counts -> base[e][b]
 //               (expert-major, so that each expert's column is contiguous)
 //   2. scan     counts[e] = sum_b (capped at the capacity when one is set),
@@ -35,10 +36,16 @@ __global__ void __launch_bounds__(kTB) dispatch_count_kernel(DispatchArgs a) {
   __syncthreads();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kTB + threadIdx.x;
   if (t < a.T) {
-    for (int j = 0; j < a.k; ++j) {
-      const int e = a.idx[t * a.k + j];
-      if (e >= 0 && e < a.N)
-        atomicAdd(&hist[e], 1);
+    // all of the token's loads first, then the counting (a load per slot
+    // followed by its atomic would wait out each load's latency in turn)
+    int e[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) e[j] = j < a.k ? a.idx[t * a.k + j] : 0;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= a.k) break;
+      if (e[j] >= 0 && e[j] < a.N)
+        atomicAdd(&hist[e[j]], 1);
       else if (a.status != nullptr)
         atomicCAS(a.status, 0, MOE_ERR_DEVICE_CHECK);
     }
@@ -132,11 +139,18 @@ __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kTB + threadIdx.x;
   const bool valid = t < a.T;
   int* my_idx = sidx + (warp * 32 + lane) * k;
-  for (int j = 0; j < k; ++j) {
-    int e = valid ? a.idx[t * k + j] : -1;
-    if (e < 0 || e >= N) e = -1;  // out-of-range indices were flagged by the count pass
-    my_idx[j] = e;
-    if (e >= 0) atomicOr(&lanes[warp * N + e], 1u << lane);
+  {
+    int ev[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) ev[j] = (valid && j < k) ? a.idx[t * k + j] : -1;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= k) break;
+      int e = ev[j];
+      if (e < 0 || e >= N) e = -1;  // out-of-range indices were flagged by the count pass
+      my_idx[j] = e;
+      if (e >= 0) atomicOr(&lanes[warp * N + e], 1u << lane);
+    }
   }
   __syncthreads();
   // per expert: exclusive scan over warps of their pair counts, plus the
@@ -166,6 +180,159 @@ __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
         continue;
       }
       const int row = a.offsets[e] + rank;
+      a.row_token[row] = static_cast<int32_t>(t);
+      a.inv[t * k + j] = row;
+    }
+  }
+}
+
+// Small batches (T*k <= kSmallPairs pairs and ceil(T/32) * N <= kSmallMasks):
+// count, scan and permute in ONE block of 1024 threads instead of three
+// launches. Tokens form groups of 32 (one warp's lanes); the block
+//   1. copies idx to shared memory and records, per (group g, expert e), the
+//      mask of lanes whose token holds e (a ballot per expert when N <= 32,
+//      else shared-memory ORs);
+//   2. scans each expert's masks over the groups (a warp per expert, shuffle
+//      scans): base[g][e] = pairs of e in groups before g, count[e] = total;
+//   3. scans the (capped) counts over experts into offsets;
+//   4. ranks each pair: base[g][e] + lower lanes of its group holding e.
+// Same rows, in the same (expert, token) order, as the multi-block path.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
+constexpr int64_t kSmallPairs = 16384;
+constexpr int64_t kSmallMasks = 8192;
+
+__global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(DispatchArgs a) {
+  extern __shared__ int sm[];
+  const int N = a.N, k = a.k;
+  const int64_t T = a.T, P = T * k;
+  const int G = static_cast<int>((T + 31) / 32);
+  int* sidx = sm;                                                  // [T*k]
+  unsigned* masks = reinterpret_cast<unsigned*>(sidx + P);         // [G][N]
+  int* base = reinterpret_cast<int*>(masks + static_cast<size_t>(G) * N);  // [G][N]
+  int* tot = base + static_cast<size_t>(G) * N;                    // [N]
+  int* off = tot + N;                                              // [N + 1]
+  __shared__ int warp_sums[kSmallWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // copy idx first (read-only loads, all in flight together), check it from
+  // shared memory afterwards: a flag write between the loads would order them
+  for (int64_t i0 = threadIdx.x; i0 < P; i0 += 8 * kSmallThreads) {
+    int v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t i = i0 + u * kSmallThreads;
+      v[u] = i < P ? __ldg(a.idx + i) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t i = i0 + u * kSmallThreads;
+      if (i < P) sidx[i] = v[u];
+    }
+  }
+  for (int64_t i = threadIdx.x; i < static_cast<int64_t>(G) * N; i += kSmallThreads) masks[i] = 0u;
+  __syncthreads();
+  if (a.status != nullptr) {
+    bool bad = false;
+    for (int64_t i = threadIdx.x; i < P; i += kSmallThreads) bad |= sidx[i] < 0 || sidx[i] >= N;
+    if (bad) atomicCAS(a.status, 0, MOE_ERR_DEVICE_CHECK);
+  }
+  // 1. lane masks per (group, expert): with N <= 32 one ballot per expert
+  //    over each lane's set of experts, else shared-memory ORs
+  const unsigned below = (1u << lane) - 1u;
+  for (int g = warp; g < G; g += kSmallWarps) {
+    const int64_t t = static_cast<int64_t>(g) * 32 + lane;
+    if (N <= 32) {
+      unsigned mine = 0u;
+      for (int j = 0; j < k; ++j) {
+        const int e = t < T ? sidx[t * k + j] : -1;
+        if (e >= 0 && e < N) mine |= 1u << e;
+      }
+      for (int e = 0; e < N; ++e) {
+        const unsigned m = __ballot_sync(0xffffffffu, (mine >> e) & 1u);
+        if (lane == 0) masks[static_cast<size_t>(g) * N + e] = m;
+      }
+    } else if (t < T) {
+      for (int j = 0; j < k; ++j) {
+        const int e = sidx[t * k + j];
+        if (e >= 0 && e < N) atomicOr(&masks[static_cast<size_t>(g) * N + e], 1u << lane);
+      }
+    }
+  }
+  __syncthreads();
+  // 2. per expert: exclusive scan of its pair counts over the groups
+  for (int e = warp; e < N; e += kSmallWarps) {
+    int carry = 0;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      const int c = g < G ? __popc(masks[static_cast<size_t>(g) * N + e]) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < G) base[static_cast<size_t>(g) * N + e] = carry + incl - c;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    // rows kept for this expert: all of them, or its first `capacity` pairs
+    if (lane == 0) tot[e] = a.cap_enabled && carry > a.capacity ? static_cast<int>(a.capacity) : carry;
+  }
+  __syncthreads();
+  // 3. exclusive scan of tot over experts: each thread a contiguous chunk
+  {
+    const int per = (N + kSmallThreads - 1) / kSmallThreads;
+    const int lo = threadIdx.x * per, hi = min(N, lo + per);
+    int local = 0;
+    for (int e = lo; e < hi; ++e) local += tot[e];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int v = warp_sums[lane];
+      int inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      warp_sums[lane] = inc - v;
+    }
+    __syncthreads();
+    int run = warp_sums[warp] + incl - local;
+    for (int e = lo; e < hi; ++e) {
+      off[e] = run;
+      a.counts[e] = tot[e];
+      a.offsets[e] = run;
+      run += tot[e];
+    }
+    if (hi == N && lo < hi) {
+      off[N] = run;
+      a.offsets[N] = run;
+    }
+  }
+  __syncthreads();
+  // 4. ranks, rows and the inverse index
+  for (int g = warp; g < G; g += kSmallWarps) {
+    const int64_t t = static_cast<int64_t>(g) * 32 + lane;
+    if (t >= T) continue;
+    for (int j = 0; j < k; ++j) {
+      const int e = sidx[t * k + j];
+      if (e < 0 || e >= N) {
+        a.inv[t * k + j] = -1;
+        continue;
+      }
+      const size_t ge = static_cast<size_t>(g) * N + e;
+      const int rank = base[ge] + __popc(masks[ge] & below);
+      if (a.cap_enabled && rank >= a.capacity) {
+        a.inv[t * k + j] = -1;  // beyond the expert's capacity: dropped
+        continue;
+      }
+      const int row = off[e] + rank;
       a.row_token[row] = static_cast<int32_t>(t);
       a.inv[t * k + j] = row;
     }
@@ -206,15 +373,27 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     if (e1 != cudaSuccess) return e1;
     return cudaMemsetAsync(a.offsets, 0, sizeof(int32_t) * (a.N + 1), stream);
   }
-  const int nb = static_cast<int>((a.T + kTB - 1) / kTB);
-  dispatch_count_kernel<<<nb, kTB, a.N * sizeof(int), stream>>>(a);
-  dispatch_scan_kernel<<<1, 1024, 0, stream>>>(a, nb);
-  const size_t smem = sizeof(int) * (2 * static_cast<size_t>(kWarps) * a.N + kWarps * 32 * a.k);
-  cudaError_t err = cudaFuncSetAttribute(dispatch_permute_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
-  dispatch_permute_kernel<<<nb, kTB, smem, stream>>>(a);
+  const int64_t pairs = a.T * a.k;
+  const int64_t groups = (a.T + 31) / 32;
+  if (pairs <= kSmallPairs && groups * a.N <= kSmallMasks) {
+    const size_t smem = sizeof(int) * (static_cast<size_t>(pairs) + 2 * static_cast<size_t>(groups) * a.N +
+                                       2 * static_cast<size_t>(a.N) + 1);
+    cudaError_t err = cudaFuncSetAttribute(dispatch_small_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    dispatch_small_kernel<<<1, kSmallThreads, smem, stream>>>(a);
+  } else {
+    const int nb = static_cast<int>((a.T + kTB - 1) / kTB);
+    dispatch_count_kernel<<<nb, kTB, a.N * sizeof(int), stream>>>(a);
+    dispatch_scan_kernel<<<1, 1024, 0, stream>>>(a, nb);
+    const size_t smem = sizeof(int) * (2 * static_cast<size_t>(kWarps) * a.N + kWarps * 32 * a.k);
+    cudaError_t err = cudaFuncSetAttribute(dispatch_permute_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    dispatch_permute_kernel<<<nb, kTB, smem, stream>>>(a);
+  }
   if (a.x_disp != nullptr) {
     const int64_t blocks = static_cast<int64_t>(num_sms()) * 8;
     const unsigned grid = static_cast<unsigned>(a.T < blocks ? a.T : blocks);
