@@ -820,12 +820,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 // W_down rows c0 + 128 r + [0,128); one MMA covers the tile's 256 output
 // columns. TMEM lane = output column; the epilogue writes back row by row.
 // A tail of 4..64 rows no longer costs a 256 x 256 MMA per K-step.
-constexpr int kPairStages = MOE_PAIR_STAGES;
-constexpr uint32_t kPairStageA = 128 * 128;
-constexpr uint32_t kPairStageB = 128 * 128;
-constexpr uint32_t kPairStageX = kSwapBoxBytes;   // tail rows of a swapped tile
-constexpr uint32_t kPairStageBytes = kPairStageA + kPairStageB + kPairStageX;
-constexpr size_t kPairDynSmem = static_cast<size_t>(kPairStages) * kPairStageBytes + 1024;
+//
+// Two K-steps per stage (KS = 2): when every reduction width is a multiple of
+// 64, each operand is also described as a 3-D tensor [K / 64][rows][64] and
+// one TMA load brings 2 x 64 columns of 128 (or 32) rows: the two canonical
+// K-major blocks of two K-steps, one after the other. Half the load
+// instructions for the same bytes; three stages of 72 KB instead of six of
+// 36 KB.
+constexpr uint32_t kPairStepA = 128 * 128;          // A rows of one K-step
+constexpr uint32_t kPairStepB = 128 * 128;          // B rows of one K-step
+constexpr uint32_t kPairStepX = kSwapBoxBytes;      // tail rows of a swapped tile
+template <int KS>
+struct PairStage {
+  static constexpr int kStages = KS == 1 ? MOE_PAIR_STAGES : 3;
+  static constexpr uint32_t A = KS * kPairStepA, B = KS * kPairStepB, X = KS * kPairStepX;
+  static constexpr uint32_t kBytes = A + B + X;
+  static constexpr size_t kDynSmem = static_cast<size_t>(kStages) * kBytes + 1024;
+};
+constexpr int kPairMaxStages = MOE_PAIR_STAGES > 3 ? MOE_PAIR_STAGES : 3;
+#ifndef MOE_PAIR_TWO_K
+#define MOE_PAIR_TWO_K 1
+#endif
+constexpr bool kPairTwoK = MOE_PAIR_TWO_K != 0;
 static_assert(kPairSwapRows <= 2 * kSwapBoxRows, "a CTA's half of a swapped tail fits one box");
 
 // Epilogue of a swapped tail of the pair kernel. Accumulator columns [0, N)
@@ -925,7 +941,7 @@ __device__ __forceinline__ TileInfo decode_pair_tile(int tile, const int* tile_s
   return ti;
 }
 
-template <int MODE>
+template <int MODE, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA0,
                              const __grid_constant__ CUtensorMap mapB0,
@@ -935,6 +951,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap mapB1u,
                              const __grid_constant__ CUtensorMap mapAs, const GemmParams p) {
   using T = __nv_bfloat16;
+  using PS = PairStage<KS>;
+  constexpr int kPairStages = PS::kStages;
+  constexpr uint32_t kPairStageA = PS::A, kPairStageB = PS::B, kPairStageBytes = PS::kBytes;
   constexpr int BK = 64;
   constexpr int BM = 256;                                  // rows per pair tile
   constexpr int BN = MODE == kSwiGLU ? 128 : 256;
@@ -943,8 +962,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t full_bar[kPairStages];
-  __shared__ __align__(8) uint64_t empty_bar[kPairStages];
+  __shared__ __align__(8) uint64_t full_bar[kPairMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kPairMaxStages];
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ uint32_t tmem_base_sh;
@@ -1035,8 +1054,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // bytes per stage of both CTAs: plain tiles A + B; swapped tails the
       // weight rows (both halves in pass A, one in pass B) and the tail box
       const uint32_t tile_tx =
-          swapped ? 2 * ((MODE == kSwiGLU ? kPairStageA + kPairStageB : kPairStageA) + kPairStageX)
-                  : 2 * (kPairStageA + kPairStageB);
+          KS * (swapped ? 2 * ((MODE == kSwiGLU ? kPairStepA + kPairStepB : kPairStepA) + kPairStepX)
+                        : 2 * (kPairStepA + kPairStepB));
+      const int n_stages = (ti.num_kb + KS - 1) / KS;
       const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
       const void* mB;
       int b_row;
@@ -1062,7 +1082,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           g4[i] = p.gather_rows[r];
         }
       }
-      for (int kb = 0; kb < ti.num_kb; ++kb) {
+      for (int ks = 0; ks < n_stages; ++ks) {
+        const int kb = ks * KS;  // first 64-column block of the stage
         bool w = true;
         if (lane == 0)
           w = mbar_wait_bounded_cluster(&empty_bar[stage], phase ^ 1u, abort_v, p.status,
@@ -1078,29 +1099,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[stage]), 0);
         if (lane == 0 && leader) mbar_arrive_expect_tx(&full_bar[stage], tile_tx);
         __syncwarp();
+        // one load of a tiled operand: a 2-D box (KS = 1) or the 3-D box of
+        // the stage's two 64-column blocks (KS = 2)
+        auto load = [&](uint8_t* dst, const void* map, int row) {
+          if (KS == 1)
+            tma_load_2d_pair(dst, map, full_leader, kb * BK, row);
+          else
+            tma_load_3d_pair(dst, map, full_leader, 0, row, kb);
+        };
         if (swapped) {
-          // tail rows into the X region (a 32-row box, or 8 gather4 lanes)
+          // tail rows into the X region (a 32-row box, or 8 gather4 lanes per block)
           if (gather) {
             if (lane < kSwapBoxRows / 4)
-              tma_gather4_pair(sX + lane * 512, mA, full_leader, kb * BK, g4[0], g4[1], g4[2],
-                               g4[3]);
+              for (int c = 0; c < KS; ++c)
+                tma_gather4_pair(sX + c * kPairStepX + lane * 512, mA, full_leader, (kb + c) * BK,
+                                 g4[0], g4[1], g4[2], g4[3]);
           } else if (lane == 0) {
-            tma_load_2d_pair(sX, &mapAs, full_leader, kb * BK, a_row);
+            load(sX, &mapAs, a_row);
           }
           if (lane == 0) {
             if (MODE == kSwiGLU) {
-              tma_load_2d_pair(sA, &mapB0, full_leader, kb * BK, w_row);    // W_gate rows
-              tma_load_2d_pair(sB, &mapB0u, full_leader, kb * BK, w_row);   // W_up rows
+              load(sA, &mapB0, w_row);    // W_gate rows
+              load(sB, &mapB0u, w_row);   // W_up rows
             } else {
-              tma_load_2d_pair(sA, &mapB0, full_leader, kb * BK, w_row);    // W_down rows
+              load(sA, &mapB0, w_row);    // W_down rows
             }
           }
         } else {
           if (gather)
-            tma_gather4_pair(sA + lane * 512, mA, full_leader, kb * BK, g4[0], g4[1], g4[2], g4[3]);
+            for (int c = 0; c < KS; ++c)
+              tma_gather4_pair(sA + c * kPairStepA + lane * 512, mA, full_leader, (kb + c) * BK,
+                               g4[0], g4[1], g4[2], g4[3]);
           if (lane == 0) {
-            if (!gather) tma_load_2d_pair(sA, mA, full_leader, kb * BK, a_row);
-            tma_load_2d_pair(sB, mB, full_leader, kb * BK, b_row);
+            if (!gather) load(sA, mA, a_row);
+            load(sB, mB, b_row);
           }
         }
         if (++stage == kPairStages) {
@@ -1131,7 +1163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * kAccCols;
-        for (int kb = 0; kb < ti.num_kb; ++kb) {
+        const int n_stages = (ti.num_kb + KS - 1) / KS;
+        for (int ks = 0; ks < n_stages; ++ks) {
           if (!mbar_wait_bounded_cluster(&full_bar[stage], phase, abort_v, p.status, p.budget_ns,
                                          MOE_ERR_TIMEOUT)) {
             ok = false;
@@ -1140,24 +1173,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + stage * kPairStageBytes);
           const uint32_t b_addr = a_addr + kPairStageA;
-          if (ti.nr > 0) {
-            // swapped tail: weights (A region; W_up in the B region) x tail rows
-            const uint32_t x_addr = b_addr + kPairStageB;
+          // a last stage of KS = 2 past the reduction width holds zero-filled
+          // columns (their products add nothing)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t xd = sw128_kmajor_desc(x_addr + kk * 32);
-              const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
-              mma_f16_pair(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), xd, idesc_swap, accum);
-              if (MODE == kSwiGLU)
-                mma_f16_pair(d_tmem + kAccCols / 2, sw128_kmajor_desc(b_addr + kk * 32), xd,
-                             idesc_swap, accum);
-            }
-          } else {
+          for (int c = 0; c < KS; ++c) {
+            const uint32_t ac = a_addr + c * kPairStepA, bc = b_addr + c * kPairStepB;
+            if (ti.nr > 0) {
+              // swapped tail: weights (A region; W_up in the B region) x tail rows
+              const uint32_t xc = b_addr + kPairStageB + c * kPairStepX;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sw128_kmajor_desc(a_addr + kk * 32);
-              const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
-              mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t xd = sw128_kmajor_desc(xc + kk * 32);
+                const uint32_t accum = (ks | c | kk) != 0 ? 1u : 0u;
+                mma_f16_pair(d_tmem, sw128_kmajor_desc(ac + kk * 32), xd, idesc_swap, accum);
+                if (MODE == kSwiGLU)
+                  mma_f16_pair(d_tmem + kAccCols / 2, sw128_kmajor_desc(bc + kk * 32), xd,
+                               idesc_swap, accum);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sw128_kmajor_desc(ac + kk * 32);
+                const uint64_t bd = sw128_kmajor_desc(bc + kk * 32);
+                mma_f16_pair(d_tmem, ad, bd, idesc, (ks | c | kk) != 0 ? 1u : 0u);
+              }
             }
           }
           mma_commit_pair(&empty_bar[stage], 0x3);
@@ -1304,6 +1343,27 @@ bool make_map(CUtensorMap* m, const void* ptr, int dtype, uint64_t inner, uint64
   return r == CUDA_SUCCESS;
 }
 
+// The same row-major [rows, inner] tensor as a 3-D tensor [inner / 64][rows][64]
+// (dims innermost first: 64 elements, rows, 64-element blocks), box = 64 x
+// box_rows x 2 with the 128-byte swizzle: one load brings two 64-column blocks
+// of box_rows rows, each block a contiguous K-major tile. Needs inner % 64 == 0
+// (a block must not run into the next row); returns false when the driver
+// does not accept the description.
+bool make_map_2k(CUtensorMap* m, const void* ptr, int dtype, uint64_t inner, uint64_t rows,
+                 uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr || dtype != MOE_BF16 || inner % 64 != 0) return false;
+  cuuint64_t gdim[3] = {64, rows, inner / 64};
+  cuuint64_t gstride[2] = {inner * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), gdim,
+                         gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int MODE, typename T, int KT = 1>
 cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid, cudaStream_t stream) {
   auto kern = grouped_gemm_kernel<MODE, T, KT>;
@@ -1322,12 +1382,12 @@ int tiles_bound(int64_t rows_routed, int n_groups, int64_t n_out, int BN, int64_
   return static_cast<int>(b < 1 ? 1 : (b > (1 << 30) ? (1 << 30) : b));
 }
 
-// Clusters of two CTAs that can be resident at once (one CTA per SM).
-int pair_clusters(const void* kern, cudaLaunchConfig_t cfg) {
-  static int cache[64][2] = {};
+// Clusters of two CTAs that can be resident at once (one CTA per SM), cached
+// per device and kernel instance (`slot`).
+int pair_clusters(const void* kern, cudaLaunchConfig_t cfg, int slot) {
+  static int cache[64][4] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  const int slot = kern == reinterpret_cast<const void*>(grouped_gemm_pair_kernel<kSwiGLU>) ? 0 : 1;
   if (dev >= 0 && dev < 64 && cache[dev][slot] > 0) return cache[dev][slot];
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
@@ -1338,10 +1398,11 @@ int pair_clusters(const void* kern, cudaLaunchConfig_t cfg) {
   return n;
 }
 
-template <int MODE>
+template <int MODE, int KS>
 cudaError_t launch_gemm_pair(const CUtensorMap* maps, const GemmParams& p, int pair_tiles,
                              cudaStream_t stream) {
-  auto kern = grouped_gemm_pair_kernel<MODE>;
+  auto kern = grouped_gemm_pair_kernel<MODE, KS>;
+  constexpr size_t kPairDynSmem = PairStage<KS>::kDynSmem;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kPairDynSmem));
   if (err != cudaSuccess) return err;
@@ -1357,7 +1418,8 @@ cudaError_t launch_gemm_pair(const CUtensorMap* maps, const GemmParams& p, int p
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(2, 1, 1);
-  int clusters = pair_clusters(reinterpret_cast<const void*>(kern), cfg);
+  int clusters = pair_clusters(reinterpret_cast<const void*>(kern), cfg,
+                               (MODE == kSwiGLU ? 0 : 1) + (KS == 2 ? 2 : 0));
   if (clusters > pair_tiles) clusters = pair_tiles;
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
@@ -1427,10 +1489,32 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   // CTA pairs (256-row tiles) pay off when experts hold many rows on average;
   // with few rows per expert the 128-row tiles waste less of the MMA.
   const bool pair = a.dtype == MOE_BF16 && R >= static_cast<int64_t>(kPairMinRowsPerExpert) * a.N;
+  // CTA pairs with two K-steps per stage when every reduction width is a
+  // multiple of 64 and the driver accepts the 3-D descriptions (else one)
+  const bool widths_2k = kPairTwoK && a.d % 64 == 0 && a.F % 64 == 0 && a.F_sh % 64 == 0;
   cudaError_t err;
   if (pair) {
-    err = launch_gemm_pair<kSwiGLU>(m, pa, tiles_bound(R, a.N, a.F, 128, sh ? a.T : 0, a.F_sh, 256),
-                                    stream);
+    const int bound = tiles_bound(R, a.N, a.F, 128, sh ? a.T : 0, a.F_sh, 256);
+    CUtensorMap m2[7];
+    bool two_k = widths_2k &&
+                 make_map_2k(&m2[1], a.W_gate, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, 128) &&
+                 make_map_2k(&m2[2], a.W_up, a.dtype, a.d, static_cast<uint64_t>(a.N) * a.F, 128);
+    if (two_k && gather) {
+      m2[0] = m[0];  // gather4 reads the 2-D map, one load per 64-column block
+      m2[6] = m[0];
+    } else if (two_k) {
+      two_k = make_map_2k(&m2[0], a.x_disp, a.dtype, a.d, R, kBM) &&
+              make_map_2k(&m2[6], a.x_disp, a.dtype, a.d, R, kSwapBoxRows);
+    }
+    if (two_k && sh) {
+      two_k = make_map_2k(&m2[3], a.h, a.dtype, a.d, a.T, kBM) &&
+              make_map_2k(&m2[4], a.Ws_gate, a.dtype, a.d, a.F_sh, 128) &&
+              make_map_2k(&m2[5], a.Ws_up, a.dtype, a.d, a.F_sh, 128);
+    } else if (two_k) {
+      m2[3] = m2[0]; m2[4] = m2[1]; m2[5] = m2[2];
+    }
+    err = two_k ? launch_gemm_pair<kSwiGLU, 2>(m2, pa, bound, stream)
+                : launch_gemm_pair<kSwiGLU, 1>(m, pa, bound, stream);
   } else {
     int grid = tiles_bound(R, a.N, a.F, 128, sh ? a.T : 0, a.F_sh);
     if (grid > sms) grid = sms;
@@ -1465,8 +1549,24 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t stream) {
   pb.n_out_shared = a.d;
   pb.out = a.scatter_token != nullptr ? a.scatter_out : a.y_rows;
   pb.out_shared = a.y_shared;
-  if (pair) return launch_gemm_pair<kDown>(m, pb, tiles_bound(R, a.N, a.d, 256, sh ? a.T : 0, a.d, 256),
-                                           stream);
+  if (pair) {
+    const int bound = tiles_bound(R, a.N, a.d, 256, sh ? a.T : 0, a.d, 256);
+    CUtensorMap m2[7];
+    bool two_k = widths_2k &&
+                 make_map_2k(&m2[0], a.act, a.dtype, a.F, R, kBM) &&
+                 make_map_2k(&m2[6], a.act, a.dtype, a.F, R, kSwapBoxRows) &&
+                 make_map_2k(&m2[1], a.W_down, a.dtype, a.F, static_cast<uint64_t>(a.N) * a.d, 128);
+    m2[2] = m2[1];
+    if (two_k && sh) {
+      two_k = make_map_2k(&m2[3], a.act_sh, a.dtype, a.F_sh, a.T, kBM) &&
+              make_map_2k(&m2[4], a.Ws_down, a.dtype, a.F_sh, a.d, 128);
+      m2[5] = m2[4];
+    } else if (two_k) {
+      m2[3] = m2[0]; m2[4] = m2[1]; m2[5] = m2[1];
+    }
+    return two_k ? launch_gemm_pair<kDown, 2>(m2, pb, bound, stream)
+                 : launch_gemm_pair<kDown, 1>(m, pb, bound, stream);
+  }
   int grid = tiles_bound(R, a.N, a.d, 256, sh ? a.T : 0, a.d);
   if (grid > sms) grid = sms;
   return a.dtype == MOE_F32 ? launch_gemm<kDown, float>(m, pb, grid, stream)

@@ -252,6 +252,18 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* map
       : "memory");
 }
 
+// 3-D tiled bulk tensor load into this CTA's shared memory, completion on a
+// pair barrier (as tma_load_2d_pair); coordinates innermost first.
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const void* map,
+                                                 uint32_t mbar_cluster, int32_t x, int32_t y,
+                                                 int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_result, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_u32(smem_result)),
