@@ -44,6 +44,10 @@ SMALL = {
     # (16 and 11 m-tiles) beside 14 groups of 329 rows down to 3, shared expert
     "skewed_groups": Workload("skewed_groups", T=2048, d=192, N=16, F=256, k=2, F_sh=128,
                               score="sigmoid", bias_zipf_s=1.1, bias_beta=0.5),
+    # 128 rows per expert on average (one CTA per 128-row tile) but skewed:
+    # groups of several m-tiles beside small ones, shared expert
+    "skewed_one_cta": Workload("skewed_one_cta", T=2048, d=192, N=16, F=256, k=1, F_sh=128,
+                               score="sigmoid", bias_zipf_s=1.1, bias_beta=0.3),
     # top-1 without a shared expert (fused combine), counts 1350 and 368 .. 76
     "skewed_groups_top1": Workload("skewed_groups_top1", T=4096, d=128, N=16, F=128, k=1,
                                    score="sigmoid", norm="none", bias_zipf_s=1.1, bias_beta=0.08),
@@ -58,7 +62,8 @@ SMALL = {
                                  score="sigmoid", wr_std=0.1),
     "softmax_bias_none": Workload("softmax_bias_none", T=333, d=128, N=32, F=128, k=3,
                                   norm="none", bias_zipf_s=1.1, bias_beta=0.05),
-    # >= 768 rows per expert: the grouped GEMM runs on CTA pairs (256-row tiles)
+    # >= 256 rows per expert on average: the grouped GEMM runs on CTA pairs
+    # (256-row tiles)
     "pair_ragged": Workload("pair_ragged", T=1700, d=256, N=2, F=384, k=1),
     "pair_shared_ragged_n": Workload("pair_shared_ragged_n", T=2100, d=192, N=2, F=320, k=1,
                                      F_sh=256, score="sigmoid", bias_zipf_s=1.1),
@@ -389,7 +394,7 @@ def test_fused_top1_forward_vs_oracle(cuda_lib, name):
 
 @pytest.mark.parametrize("name", ["ragged_softmax_top2", "sigmoid_bias_shared", "many_experts",
                                   "pair_shared_ragged_n", "multi_mtile_ragged_n", "pair_half_tails",
-                                  "pair_mixed_tails", "skewed_groups"])
+                                  "pair_mixed_tails", "skewed_groups", "skewed_one_cta"])
 def test_gather_ffn_equals_dispatched_copy(cuda_lib, name):
     """The grouped GEMM fed by TMA gather4 from h (the moe_forward path) gives
     bitwise the same rows as the one fed by the dispatched copy x_disp."""
@@ -418,7 +423,7 @@ def test_pair_workloads_cover_both_tail_kinds(cuda_lib, name):
     w = SMALL[name]
     r = run_staged(api.config_for(w), gpu_inputs(synth.make_inputs(w, seed=0, device="cpu")))
     c = np_i(r["counts"])
-    assert c.sum() >= 768 * w.N, "the grouped GEMM would not run on CTA pairs"
+    assert c.sum() >= 256 * w.N, "the grouped GEMM would not run on CTA pairs"
     rem = c % 256
     assert ((rem >= 1) & (rem <= 128)).any() and (rem > 128).any(), c.tolist()
 
@@ -510,7 +515,7 @@ def test_expert_ffn_group_sizes_around_tile_boundaries(cuda_lib):
 
 
 def test_pair_kernel_tails_around_swap_boundaries(cuda_lib):
-    """Groups large enough for the CTA-pair kernel (>= 768 rows per expert on
+    """Groups large enough for the CTA-pair kernel (>= 256 rows per expert on
     average), whose last 256-row tiles hold 1..250 rows: tails of at most 64
     rows run with swapped operands (weights on the M=256 side, the tail rows
     as N split over the pair), the others as plain tiles. One group is a
@@ -520,7 +525,7 @@ def test_pair_kernel_tails_around_swap_boundaries(cuda_lib):
     rows."""
     sizes = [1025, 1040, 1041, 1057, 1087, 64, 1088, 1089, 1274, 0, 1040, 17]
     N, R, d, F = len(sizes), sum(sizes), 320, 384
-    assert R >= 768 * N, "the grouped GEMM must run on CTA pairs"
+    assert R >= 256 * N, "the grouped GEMM must run on CTA pairs"
     w = Workload("pair_tails", T=R, d=d, N=N, F=F, k=1, F_sh=128, wd_scale=0.5)
     cfg = api.config_for(w)
     inp = synth.make_inputs(w, seed=13, device="cpu")

@@ -68,7 +68,7 @@ namespace {
 #define MOE_PAIR_STAGES 6
 #endif
 #ifndef MOE_PAIR_MIN_ROWS
-#define MOE_PAIR_MIN_ROWS 768
+#define MOE_PAIR_MIN_ROWS 256
 #endif
 
 constexpr int kBM = 128;
