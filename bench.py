@@ -45,9 +45,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 def kernels_per_forward(w) -> int:
     """Launches of one moe_forward: route 1 (one GEMM with the top-k in its
     epilogue, or the CUDA-core kernel) or 2 (split logits GEMM + selection,
-    when the batch has too few 128-token tiles to fill the GPU), dispatch 4,
-    grouped GEMM 2, combine 1 (top-1 without a shared expert: the combine
-    happens in the down pass)."""
+    when the batch has too few 128-token tiles to fill the GPU), dispatch 2
+    (one block for count, scan and permute on small batches, plus the gather)
+    or 4, grouped GEMM 2, combine 1 (top-1 without a shared expert: the
+    combine happens in the down pass)."""
     route = 1
     if w.dtype == "bf16" and w.N <= 256:
         tiles = (w.T + 127) // 128
@@ -56,8 +57,10 @@ def kernels_per_forward(w) -> int:
         kb_per = (kb_total + s - 1) // s
         if (kb_total + kb_per - 1) // kb_per > 1:
             route = 2
+    small = w.T * w.k <= 16384 and ((w.T + 31) // 32) * w.N <= 8192
+    dispatch = 2 if small else 4
     combine = 0 if (w.k == 1 and w.F_sh == 0) else 1
-    return route + 4 + 2 + combine
+    return route + dispatch + 2 + combine
 
 
 # ------------------------------------------------------------ host logic ---

@@ -35,6 +35,7 @@ def test_clock_record_takes_reasons_from_the_throttle_counters():
 
 def test_launches_per_forward_follow_the_router_plan():
     W = synth.WORKLOADS
-    assert bench.kernels_per_forward(W["mixtral_prefill"]) == 9     # split router
+    assert bench.kernels_per_forward(W["mixtral_prefill"]) == 7     # split router, one-block dispatch
     assert bench.kernels_per_forward(W["switch_top1"]) == 7         # fused router, fused combine
-    assert bench.kernels_per_forward(W["tiny_fp32"]) == 8           # CUDA-core router
+    assert bench.kernels_per_forward(W["tiny_fp32"]) == 6           # CUDA-core router, one-block dispatch
+    assert bench.kernels_per_forward(W["fine_grained_shared"]) == 9  # split router, four-launch dispatch

@@ -87,9 +87,11 @@ WORKLOADS = {
 
 
 # Reduced cases of the same kernels for profiler captures: weights still
-# larger than L2, a few hundred MB of activations.
+# larger than L2, a few hundred MB of activations. prof_prefill holds 2 of the
+# Mixtral-shaped prefill's 8 experts with the same ~1024 rows each, so its
+# grouped-GEMM traffic is a quarter of the full batch's.
 PROFILE_WORKLOADS = {
-    "prof_prefill": Workload("prof_prefill", T=2048, d=4096, N=2, F=14336, k=2),
+    "prof_prefill": Workload("prof_prefill", T=1024, d=4096, N=2, F=14336, k=2),
     "prof_fine_grained": Workload("prof_fine_grained", T=2048, d=7168, N=64, F=2048, k=8,
                                   F_sh=2048, score="sigmoid", bias_zipf_s=1.1),
     "prof_switch": Workload("prof_switch", T=16384, d=2048, N=128, F=768, k=1, norm="none"),
