@@ -433,7 +433,7 @@ __device__ __forceinline__ void swap_epilogue(uint32_t tbase, const TileInfo& ti
         if (MODE == kSwiGLU) {
           if (c0 < ti.ncols)
             static_cast<bf*>(p.out)[static_cast<size_t>(r0 + r) * p.n_out + c0] =
-                __float2bfloat16_rn(v0 / (1.0f + __expf(-v0)) * v1);
+                __float2bfloat16_rn(__fdividef(v0, 1.0f + __expf(-v0)) * v1);
         } else {
           size_t base = static_cast<size_t>(r0 + r) * p.n_out;
           float scale = 1.f;
@@ -762,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) {
               const float gv = __uint_as_float(gr[i]);
               const float uv = __uint_as_float(ur[i]);
-              act[i] = gv / (1.0f + __expf(-gv)) * uv;
+              act[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
             }
             store32(out + c, act, cols_left - c);
           }
@@ -872,7 +872,7 @@ __device__ __forceinline__ void pair_swap_epilogue(uint32_t tbase, const TileInf
         if (MODE == kSwiGLU) {
           const float v1 = __uint_as_float(d1[j]);
           static_cast<bf*>(p.out)[static_cast<size_t>(r0 + r) * p.n_out + o] =
-              __float2bfloat16_rn(v0 / (1.0f + __expf(-v0)) * v1);
+              __float2bfloat16_rn(__fdividef(v0, 1.0f + __expf(-v0)) * v1);
         } else {
           size_t base = static_cast<size_t>(r0 + r) * p.n_out;
           float scale = 1.f;
@@ -1262,7 +1262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) {
               const float gv = __uint_as_float(gr[i]);
               const float uv = __uint_as_float(ur[i]);
-              act[i] = gv / (1.0f + __expf(-gv)) * uv;
+              act[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
             }
             store32(out + c, act, cols_left - c);
           }
