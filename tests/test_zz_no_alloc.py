@@ -37,9 +37,11 @@ def test_noalloc_dispatch_matches_workspace_dispatch_on_consecutive_calls():
     dev = "cuda"
     # calls in a row with different shapes, each reusing the array the one
     # before filled: the last fills the array exactly (ceil(65536 / 256) *
-    # 1024 = 262144 entries), the third skips the row gather (x_disp NULL)
+    # 1024 = 262144 entries), the third skips the row gather (x_disp NULL),
+    # the fourth is small enough for the one-block count/scan/permute
     cases = ((5000, 256, 8, 64, 1, True), (777, 1024, 4, 128, 2, True),
-             (3000, 64, 6, 32, 3, False), (65536, 1024, 2, 16, 4, True))
+             (3000, 64, 6, 32, 3, False), (1000, 8, 2, 64, 5, True),
+             (65536, 1024, 2, 16, 4, True))
     for T, N, k, d, seed, gather in cases:
         cfg = api.make_config(T, d, N, k, 64)
         idx, h = _case(T, N, k, d, seed)

@@ -46,19 +46,25 @@ __device__ __forceinline__ uint4 pack(const float (&f)[4], float*) {
 // token's rows and gates once and share them by shuffles; the warp then walks
 // the row's 16-byte vectors 32 * U at a time (lane l takes v0 + l + 32 u), so
 // that U loads per slot and lane are in flight, accumulating in slot order.
+constexpr int kCombineU = 4;
+
+// `wpt` warps share a token (small batches): warp part p of a token takes the
+// row's chunks of 32 * U vectors p, p + wpt, ...; each output vector still
+// comes from one lane with the same slot-order arithmetic.
 template <typename T>
-__global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+__global__ void __launch_bounds__(256) combine_kernel(CombineArgs a, int wpt) {
   constexpr int V = 16 / sizeof(T);
-  constexpr int U = 4;
+  constexpr int U = kCombineU;
   const int nvec = a.d / V;
   const uint4* Y = static_cast<const uint4*>(a.y_rows);
   const uint4* S = static_cast<const uint4*>(a.y_shared);
   uint4* O = static_cast<uint4*>(a.out);
   const int64_t R = a.T * a.k;
   const int lane = threadIdx.x & 31;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       t < a.T; t += warps) {
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int part = static_cast<int>(gw % wpt);
+  const int64_t tokens_per_pass = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5) / wpt;
+  for (int64_t t = gw / wpt; t < a.T; t += tokens_per_pass) {
     // slot `lane`: first vector of its row (-1 = none; only rows moe_dispatch
     // wrote are read) and its gate
     int64_t my_row = -1;
@@ -71,7 +77,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
       }
     }
     // the same trip count on every lane: the shuffles below need the whole warp
-    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+    for (int v0 = part * 32 * U; v0 < nvec; v0 += wpt * 32 * U) {
       float acc[U][V];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -116,14 +122,24 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
-  // 8 warps (tokens) per block, up to 8 blocks per SM
-  const int64_t need = (a.T + 7) / 8;
-  const int64_t blocks = static_cast<int64_t>(num_sms()) * 8;
+  // a warp per token; on batches too small to give every SM a block of 8
+  // warps, up to one warp per chunk of 32 * U vectors of the row
+  const int V = a.dtype == MOE_F32 ? 4 : 8;
+  const int64_t chunks = (a.d / V + 32 * kCombineU - 1) / (32 * kCombineU);
+  const int64_t target = static_cast<int64_t>(num_sms()) * 8;
+  int64_t wpt = (target + a.T - 1) / a.T;
+  if (wpt > chunks) wpt = chunks;
+  if (wpt < 1) wpt = 1;
+  // 8 warps per block, up to 8 blocks per SM; the grid holds whole tokens
+  const int64_t need = (a.T * wpt + 7) / 8;
+  int64_t blocks = static_cast<int64_t>(num_sms()) * 8;
+  blocks = blocks / wpt * wpt;  // 8 * blocks warps: a multiple of wpt
+  if (blocks < wpt) blocks = wpt;
   const unsigned grid = static_cast<unsigned>(need < blocks ? need : blocks);
   if (a.dtype == MOE_F32)
-    combine_kernel<float><<<grid, 256, 0, stream>>>(a);
+    combine_kernel<float><<<grid, 256, 0, stream>>>(a, static_cast<int>(wpt));
   else
-    combine_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a);
+    combine_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a, static_cast<int>(wpt));
   return cudaGetLastError();
 }
 
