@@ -62,6 +62,12 @@ SMALL = {
                                  score="sigmoid", wr_std=0.1),
     "softmax_bias_none": Workload("softmax_bias_none", T=333, d=128, N=32, F=128, k=3,
                                   norm="none", bias_zipf_s=1.1, bias_beta=0.05),
+    # reduction widths that are not multiples of 64 (d = 136, F = 200): the
+    # CTA-pair kernel loads one K-step per stage and both kernels zero-fill the
+    # last partial K-block
+    "pair_one_kstep": Workload("pair_one_kstep", T=1200, d=136, N=2, F=200, k=1, F_sh=72,
+                               score="sigmoid", bias_zipf_s=1.1, bias_beta=0.3),
+    "one_cta_odd_widths": Workload("one_cta_odd_widths", T=300, d=136, N=8, F=200, k=2),
     # >= 256 rows per expert on average: the grouped GEMM runs on CTA pairs
     # (256-row tiles)
     "pair_ragged": Workload("pair_ragged", T=1700, d=256, N=2, F=384, k=1),
