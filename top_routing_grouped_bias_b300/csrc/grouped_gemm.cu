@@ -263,6 +263,62 @@ __device__ __forceinline__ void store32(__nv_bfloat16* dst, const float (&f)[32]
     }
   }
 }
+// 32 fp32 values as 16 bf16x2 words (round to nearest even).
+__device__ __forceinline__ void pack_bf16x32(const float (&f)[32], uint32_t* w) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+}
+
+// One exchange step of a 4 x 4 transpose of 32-byte pieces inside each group
+// of four lanes: a lane whose bit `m` is clear keeps piece i0 and receives
+// the partner's piece i0 into slot i1; a lane with the bit set keeps piece i1
+// and receives the partner's piece i1 into slot i0.
+template <int M>
+__device__ __forceinline__ void exchange_pieces(uint32_t (&w)[32], bool bit) {
+#pragma unroll
+  for (int i0 = 0; i0 < 4; ++i0) {
+    if (i0 & M) continue;
+    const int i1 = i0 | M;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t send = bit ? w[8 * i0 + t] : w[8 * i1 + t];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, M);
+      if (bit)
+        w[8 * i0 + t] = recv;
+      else
+        w[8 * i1 + t] = recv;
+    }
+  }
+}
+
+// A warp holds 32 rows x 64 bf16 columns, one row per lane, as four 32-byte
+// pieces w[8q, 8q + 8). After a 4 x 4 transpose of the pieces inside each
+// group of four lanes, lane 4g + q holds piece q of rows 4g .. 4g + 3, and
+// each of four 32-byte stores per lane writes whole 128-byte row segments
+// (eight rows per instruction) instead of one 16-byte piece of 32 rows.
+// `row_ptr` is this lane's output row at the block's first column (null for
+// a row past the tile), 32-byte aligned; `valid` = columns left in the rows,
+// a multiple of 16.
+__device__ __forceinline__ void store_rows64(uint32_t (&w)[32], __nv_bfloat16* row_ptr,
+                                             int valid, int lane) {
+  exchange_pieces<1>(w, (lane & 1) != 0);
+  exchange_pieces<2>(w, (lane & 2) != 0);
+  const int q = lane & 3;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(__shfl_sync(
+        0xffffffffu, reinterpret_cast<uintptr_t>(row_ptr), (lane & ~3) | r));
+    if (dst != nullptr && q * 16 < valid)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + q * 16),
+                   "r"(w[8 * r]), "r"(w[8 * r + 1]), "r"(w[8 * r + 2]), "r"(w[8 * r + 3]),
+                   "r"(w[8 * r + 4]), "r"(w[8 * r + 5]), "r"(w[8 * r + 6]), "r"(w[8 * r + 7])
+                   : "memory");
+  }
+}
+
 __device__ __forceinline__ void store32(float* dst, const float (&f)[32], int valid) {
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -1247,9 +1303,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         out = static_cast<T*>(p.out) + static_cast<size_t>(tok) * p.n_out;
       }
       out += col0;
+      // whole 128-byte row segments per store when every row starts on a
+      // 32-byte boundary
+      const bool wide = ((dense ? p.n_out_shared : p.n_out) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(dense ? p.out_shared : p.out) & 31) == 0;
       if (ti.nr > 0) {
         // swapped tail: TMEM lane = output column 256 n + 128 rank + lane_row
         pair_swap_epilogue<MODE>(tbase, ti, row_in_tile, static_cast<int>(rank), p);
+      } else if (wide) {
+        constexpr int kCols = MODE == kSwiGLU ? 128 : 256;
+#pragma unroll 1
+        for (int c = 0; c < kCols; c += 64) {
+          uint32_t w[32];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float f[32];
+            if (MODE == kSwiGLU) {
+              uint32_t gr[32], ur[32];
+              tmem_ld32_sync(tbase + c + 32 * h, gr);
+              tmem_ld32_sync(tbase + 128 + c + 32 * h, ur);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float gv = __uint_as_float(gr[i]);
+                f[i] = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(ur[i]);
+              }
+            } else {
+              uint32_t v[32];
+              tmem_ld32_sync(tbase + c + 32 * h, v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]) * scale;
+            }
+            pack_bf16x32(f, w + 16 * h);
+          }
+          if (c < cols_left)  // the same for the whole warp
+            store_rows64(w, row_ok ? out + c : nullptr, cols_left - c, lane);
+        }
       } else if (MODE == kSwiGLU) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
