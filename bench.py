@@ -451,6 +451,13 @@ def summarize(w, m, args, world):
                  "algorithmic_flops": work["gemm_flops"], "algorithmic_bytes": gb,
                  "avg_ms": round(gemm_ms, 4),
                  "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})"})
+    mhz, max_mhz = m["clocks"].get("sm_mhz"), m["clocks"].get("sm_max_mhz")
+    if roof["bound"] == "tensor" and mhz and max_mhz:
+        # context only: the burst peak scaled to the median SM clock sampled
+        # in the timed region (under the power cap the clock sets the rate)
+        burst = peaks["bf16_tflops"] / (2.0 if w.dtype == "f32" else 1.0)
+        roof["sampled_sm_mhz"] = mhz
+        roof["frac_of_burst_at_sampled_clock"] = round(gemm_tflops / (burst * mhz / max_mhz), 4)
     sb = stage_bytes(w)
     stages = {}
     for name in ("route", "dispatch", "grouped_gemm", "combine"):

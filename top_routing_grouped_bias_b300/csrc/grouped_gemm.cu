@@ -373,6 +373,53 @@ __device__ __forceinline__ void route_epilogue(uint32_t tbase, int64_t row, bool
   top.init();
   float m = -INFINITY;
   float* zrow = r.logits_out != nullptr ? r.logits_out + row * N : nullptr;
+  if (softmax && !bias && r.norm == MOE_NORM_NONE) {
+    // selection on z alone and gates p_i = exp(z_i - m) / sum_j exp(z_j - m):
+    // one pass over the accumulator, the sum of exponentials kept relative
+    // to the running maximum and rescaled when a chunk raises it
+    float s = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < n_pad; c += 32) {
+      uint32_t v[32];
+      tmem_ld32_sync(tbase + c, v);
+      if (valid) {
+        float z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = c + i;
+          z[i] = e < N ? __uint_as_float(v[i]) + (r.b_r != nullptr ? r.b_r[e] : 0.f) : -INFINITY;
+          if (e < N && zrow != nullptr) zrow[e] = z[i];
+        }
+        float cm[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          cm[i] = fmaxf(fmaxf(z[4 * i], z[4 * i + 1]), fmaxf(z[4 * i + 2], z[4 * i + 3]));
+        const float mc = fmaxf(fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3])),
+                               fmaxf(fmaxf(cm[4], cm[5]), fmaxf(cm[6], cm[7])));
+        if (mc > m) {
+          s *= __expf(m - mc);  // 0 on the first chunk (m = -inf)
+          m = mc;
+        }
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) part[i & 3] += __expf(z[i] - m);
+        s += (part[0] + part[1]) + (part[2] + part[3]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c + i < N) top.push(z[i], c + i, z[i]);
+      }
+    }
+    if (!valid) return;
+    const int k = r.k;
+#pragma unroll
+    for (int j = 0; j < KT; ++j) {
+      if (j < k) {
+        r.idx[row * k + j] = top.i[j] == 0x7fffffff ? 0 : top.i[j];
+        r.gate[row * k + j] = expf(top.z[j] - m) / s;
+      }
+    }
+    return;
+  }
 #pragma unroll 1
   for (int c = 0; c < n_pad; c += 32) {
     uint32_t v[32];

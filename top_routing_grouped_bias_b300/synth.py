@@ -94,7 +94,7 @@ PROFILE_WORKLOADS = {
     "prof_prefill": Workload("prof_prefill", T=1024, d=4096, N=2, F=14336, k=2),
     "prof_fine_grained": Workload("prof_fine_grained", T=2048, d=7168, N=64, F=2048, k=8,
                                   F_sh=2048, score="sigmoid", bias_zipf_s=1.1),
-    "prof_switch": Workload("prof_switch", T=16384, d=2048, N=128, F=768, k=1, norm="none"),
+    "prof_switch": Workload("prof_switch", T=16384, d=2048, N=32, F=768, k=1, norm="none"),
     # the named batches' T, d, N, k, scoring and bias with narrow experts:
     # h and W_r are drawn first, so the routing, dispatch and combine see the
     # same data as the full workloads while the device holds a few hundred MB
