@@ -527,9 +527,23 @@ __device__ __forceinline__ void swap_epilogue(uint32_t tbase, const TileInfo& ti
     uint32_t d0[32], d1[32];
     tmem_ld32_sync(tbase + c, d0);
     tmem_ld32_sync(tbase + kAccCols / 2 + c, d1);
+    // fused combine: lane l reads the token and gate of the chunk's row c + l
+    // once; the rows' values are then passed round by shuffles
+    int lane_tok = 0;
+    float lane_gate = 1.f;
+    if (MODE == kDown && p.scatter_token != nullptr && c + (lane_row & 31) < ti.rv) {
+      lane_tok = p.scatter_token[r0 + c + (lane_row & 31)];
+      lane_gate = p.scatter_gate[lane_tok];
+    }
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int r = c + j;
+      int tok = 0;
+      float scale = 1.f;
+      if (MODE == kDown && p.scatter_token != nullptr) {
+        tok = __shfl_sync(0xffffffffu, lane_tok, j);
+        scale = __shfl_sync(0xffffffffu, lane_gate, j);
+      }
       if (r < ti.rv) {
         const float v0 = __uint_as_float(d0[j]);
         const float v1 = __uint_as_float(d1[j]);
@@ -538,13 +552,8 @@ __device__ __forceinline__ void swap_epilogue(uint32_t tbase, const TileInfo& ti
             static_cast<bf*>(p.out)[static_cast<size_t>(r0 + r) * p.n_out + c0] =
                 __float2bfloat16_rn(__fdividef(v0, 1.0f + __expf(-v0)) * v1);
         } else {
-          size_t base = static_cast<size_t>(r0 + r) * p.n_out;
-          float scale = 1.f;
-          if (p.scatter_token != nullptr) {
-            const int tok = p.scatter_token[r0 + r];
-            scale = p.scatter_gate[tok];
-            base = static_cast<size_t>(tok) * p.n_out;
-          }
+          const size_t base = p.scatter_token != nullptr ? static_cast<size_t>(tok) * p.n_out
+                                                         : static_cast<size_t>(r0 + r) * p.n_out;
           bf* o = static_cast<bf*>(p.out) + base;
           if (c0 < ti.ncols) o[c0] = __float2bfloat16_rn(v0 * scale);
           if (c1 < ti.ncols) o[c1] = __float2bfloat16_rn(v1 * scale);
@@ -812,12 +821,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
                                     : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
       set_swap<MODE, T>(ti, p);
-      if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_v, p.status, p.budget_ns,
-                             MOE_ERR_TIMEOUT))
-        break;
-      tc_fence_after();
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc) * kAccCols;
       const int row = ti.m_blk * kBM + row_in_tile;
       const bool row_ok = row < ti.rows;
       const int col0 = ti.n_blk * BN;
@@ -826,12 +829,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       T* out = dense ? static_cast<T*>(p.out_shared) + static_cast<size_t>(row) * p.n_out_shared
                      : static_cast<T*>(p.out) + static_cast<size_t>(ti.row0 + row) * p.n_out;
       float scale = 1.f;
-      if (MODE == kDown && p.scatter_token != nullptr && !dense && row_ok) {
+      // the fused combine's token and gate are read before the wait for the
+      // accumulator, so that their latency overlaps it
+      if (MODE == kDown && p.scatter_token != nullptr && !dense && row_ok && ti.nr == 0) {
         const int tok = p.scatter_token[ti.row0 + row];
         scale = p.scatter_gate[tok];
         out = static_cast<T*>(p.out) + static_cast<size_t>(tok) * p.n_out;
       }
       out += col0;
+      if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_v, p.status, p.budget_ns,
+                             MOE_ERR_TIMEOUT))
+        break;
+      tc_fence_after();
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc) * kAccCols;
       if (ti.nr > 0) {
         // swapped tile: this thread's TMEM lane is one output column (a row
         // of the weight tile), its TMEM columns are the tile's rows
@@ -967,9 +978,23 @@ __device__ __forceinline__ void pair_swap_epilogue(uint32_t tbase, const TileInf
     uint32_t d0[32], d1[32];
     tmem_ld32_sync(tbase + c, d0);
     if (MODE == kSwiGLU) tmem_ld32_sync(tbase + kAccCols / 2 + c, d1);
+    // fused combine: lane l reads the token and gate of the chunk's row c + l
+    // once; the rows' values are then passed round by shuffles
+    int lane_tok = 0;
+    float lane_gate = 1.f;
+    if (MODE == kDown && p.scatter_token != nullptr && c + (lane_row & 31) < ti.rv) {
+      lane_tok = p.scatter_token[r0 + c + (lane_row & 31)];
+      lane_gate = p.scatter_gate[lane_tok];
+    }
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int r = c + j;
+      int tok = 0;
+      float scale = 1.f;
+      if (MODE == kDown && p.scatter_token != nullptr) {
+        tok = __shfl_sync(0xffffffffu, lane_tok, j);
+        scale = __shfl_sync(0xffffffffu, lane_gate, j);
+      }
       if (r < ti.rv && o < ti.ncols) {
         const float v0 = __uint_as_float(d0[j]);
         if (MODE == kSwiGLU) {
@@ -977,13 +1002,8 @@ __device__ __forceinline__ void pair_swap_epilogue(uint32_t tbase, const TileInf
           static_cast<bf*>(p.out)[static_cast<size_t>(r0 + r) * p.n_out + o] =
               __float2bfloat16_rn(__fdividef(v0, 1.0f + __expf(-v0)) * v1);
         } else {
-          size_t base = static_cast<size_t>(r0 + r) * p.n_out;
-          float scale = 1.f;
-          if (p.scatter_token != nullptr) {
-            const int tok = p.scatter_token[r0 + r];
-            scale = p.scatter_gate[tok];
-            base = static_cast<size_t>(tok) * p.n_out;
-          }
+          const size_t base = p.scatter_token != nullptr ? static_cast<size_t>(tok) * p.n_out
+                                                         : static_cast<size_t>(r0 + r) * p.n_out;
           static_cast<bf*>(p.out)[base + o] = __float2bfloat16_rn(v0 * scale);
         }
       }
@@ -1330,12 +1350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = cluster_id; tile < total; tile += n_clusters) {
       const TileInfo ti = decode_pair_tile<MODE, BN, BK>(tile, tile_start, grp_off, G, p);
-      if (!mbar_wait_bounded_cluster(&tfull_bar[acc], acc_phase, abort_v, p.status, p.budget_ns,
-                                     MOE_ERR_TIMEOUT))
-        break;
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                             static_cast<uint32_t>(acc) * kAccCols;
       const int row = ti.m_blk * BM + static_cast<int>(rank) * 128 + row_in_tile;
       const bool row_ok = row < ti.rows;
       const int col0 = ti.n_blk * BN;
@@ -1344,12 +1358,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       T* out = dense ? static_cast<T*>(p.out_shared) + static_cast<size_t>(row) * p.n_out_shared
                      : static_cast<T*>(p.out) + static_cast<size_t>(ti.row0 + row) * p.n_out;
       float scale = 1.f;
-      if (MODE == kDown && p.scatter_token != nullptr && !dense && row_ok) {
+      // the fused combine's token and gate are read before the wait for the
+      // accumulator, so that their latency overlaps it
+      if (MODE == kDown && p.scatter_token != nullptr && !dense && row_ok && ti.nr == 0) {
         const int tok = p.scatter_token[ti.row0 + row];
         scale = p.scatter_gate[tok];
         out = static_cast<T*>(p.out) + static_cast<size_t>(tok) * p.n_out;
       }
       out += col0;
+      if (!mbar_wait_bounded_cluster(&tfull_bar[acc], acc_phase, abort_v, p.status, p.budget_ns,
+                                     MOE_ERR_TIMEOUT))
+        break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(acc) * kAccCols;
       // whole 128-byte row segments per store when every row starts on a
       // 32-byte boundary
       const bool wide = ((dense ? p.n_out_shared : p.n_out) & 15) == 0 &&
