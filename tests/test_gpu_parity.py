@@ -421,6 +421,54 @@ def test_gather_ffn_equals_dispatched_copy(cuda_lib, name):
         assert torch.equal(ysh, r["y_sh"])
 
 
+def _offset_view(like: torch.Tensor, elems: int) -> torch.Tensor:
+    """A tensor shaped like `like` that starts `elems` elements into a larger
+    allocation (16 bytes for 8 bf16 elements)."""
+    buf = torch.empty(like.numel() + elems, dtype=like.dtype, device=like.device)
+    v = buf[elems:].view(like.shape)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+@pytest.mark.parametrize("name", ["pair_half_tails", "pair_shared_ragged_n", "skewed_one_cta"])
+def test_expert_ffn_into_16_byte_aligned_outputs(cuda_lib, name):
+    """Output rows that start on a 16-byte but not a 32-byte boundary take the
+    per-lane 16-byte stores instead of the 32-byte row-segment stores; the
+    values are bitwise those written to aligned buffers."""
+    w = SMALL[name]
+    cfg = api.config_for(w)
+    inp = gpu_inputs(synth.make_inputs(w, seed=12, device="cpu"))
+    r = run_staged(cfg, inp)
+    ws = api.alloc_workspace(cfg, "cuda")
+    y = _offset_view(r["y_rows"], 8)
+    ysh = _offset_view(r["y_sh"], 8) if w.F_sh else None
+    api.moe_expert_ffn(cfg, r["x_disp"], r["offsets"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                       y, inp["h"], inp.get("Ws_gate"), inp.get("Ws_up"), inp.get("Ws_down"),
+                       ysh, ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    assert torch.equal(y, r["y_rows"])
+    if w.F_sh:
+        assert torch.equal(ysh, r["y_sh"])
+
+
+@pytest.mark.parametrize("name", ["pair_mixed_tails", "skewed_groups_top1"])
+def test_fused_top1_forward_into_16_byte_aligned_output(cuda_lib, name):
+    """The fused top-1 combine writes g * y to token rows of an output that
+    starts 16 bytes past a 32-byte boundary: bitwise the aligned result."""
+    w = SMALL[name]
+    cfg = api.config_for(w)
+    inp = gpu_inputs(synth.make_inputs(w, seed=13, device="cpu"))
+    a = run_forward(cfg, inp)
+    ws = api.alloc_workspace(cfg, "cuda")
+    outs = api.alloc_outputs(cfg, "cuda", torch.bfloat16)
+    outs["out"] = _offset_view(outs["out"], 8)
+    api.forward(cfg, inp, outs, ws)
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == api.MOE_OK
+    assert torch.equal(outs["out"], a["out"])
+
+
 @pytest.mark.parametrize("name", ["pair_half_tails", "pair_mixed_tails"])
 def test_pair_workloads_cover_both_tail_kinds(cuda_lib, name):
     """The two pair workloads above must keep exercising what they were chosen
