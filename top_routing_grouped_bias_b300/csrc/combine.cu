@@ -45,13 +45,16 @@ __device__ __forceinline__ uint4 pack(const float (&f)[4], float*) {
 // A warp per token (warps stride over the tokens): lanes < k fetch the
 // token's rows and gates once and share them by shuffles; the warp then walks
 // the row's 16-byte vectors 32 * U at a time (lane l takes v0 + l + 32 u), so
-// that U loads per slot and lane are in flight, accumulating in slot order.
+// that U loads per slot and lane, for two slots at a time, are in flight,
+// accumulating in slot order.
 constexpr int kCombineU = 4;
 
 // `wpt` warps share a token (small batches): warp part p of a token takes the
 // row's chunks of 32 * U vectors p, p + wpt, ...; each output vector still
 // comes from one lane with the same slot-order arithmetic.
-template <typename T>
+// kPair: two slots per step (k >= 2); top-1 keeps one, which needs fewer
+// registers and so more warps per SM.
+template <typename T, bool kPair>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a, int wpt) {
   constexpr int V = 16 / sizeof(T);
   constexpr int U = kCombineU;
@@ -89,23 +92,59 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a, int wpt) {
           for (int q = 0; q < V; ++q) acc[u][q] = 0.f;
         }
       }
-      for (int j = 0; j < a.k; ++j) {
-        const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
-        const float g = __shfl_sync(0xffffffffu, my_g, j);
-        if (row < 0) continue;
-        uint4 y[U];
+      if constexpr (kPair) {
+        // two slots per step: both rows' loads are in flight before either is
+        // accumulated, and slot j is still added before slot j + 1
+        for (int j = 0; j < a.k; j += 2) {
+          const bool two = j + 1 < a.k;  // the same for the whole warp
+          const int64_t row0 = __shfl_sync(0xffffffffu, my_row, j);
+          const float g0 = __shfl_sync(0xffffffffu, my_g, j);
+          int64_t row1 = __shfl_sync(0xffffffffu, my_row, two ? j + 1 : j);
+          const float g1 = __shfl_sync(0xffffffffu, my_g, two ? j + 1 : j);
+          if (!two) row1 = -1;
+          uint4 y0[U], y1[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = v0 + lane + 32 * u;
-          if (v < nvec) y[u] = Y[row + v];
+          for (int u = 0; u < U; ++u) {
+            const int v = v0 + lane + 32 * u;
+            if (row0 >= 0 && v < nvec) y0[u] = Y[row0 + v];
+            if (row1 >= 0 && v < nvec) y1[u] = Y[row1 + v];
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            if (v0 + lane + 32 * u < nvec) {
+              float f[V];
+              if (row0 >= 0) {
+                unpack(y0[u], f, static_cast<T*>(nullptr));
+#pragma unroll
+                for (int q = 0; q < V; ++q) acc[u][q] = fmaf(g0, f[q], acc[u][q]);
+              }
+              if (row1 >= 0) {
+                unpack(y1[u], f, static_cast<T*>(nullptr));
+#pragma unroll
+                for (int q = 0; q < V; ++q) acc[u][q] = fmaf(g1, f[q], acc[u][q]);
+              }
+            }
+          }
         }
+      } else {
+        for (int j = 0; j < a.k; ++j) {
+          const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
+          const float g = __shfl_sync(0xffffffffu, my_g, j);
+          if (row < 0) continue;
+          uint4 y[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if (v0 + lane + 32 * u < nvec) {
-            float f[V];
-            unpack(y[u], f, static_cast<T*>(nullptr));
+          for (int u = 0; u < U; ++u) {
+            const int v = v0 + lane + 32 * u;
+            if (v < nvec) y[u] = Y[row + v];
+          }
 #pragma unroll
-            for (int q = 0; q < V; ++q) acc[u][q] = fmaf(g, f[q], acc[u][q]);
+          for (int u = 0; u < U; ++u) {
+            if (v0 + lane + 32 * u < nvec) {
+              float f[V];
+              unpack(y[u], f, static_cast<T*>(nullptr));
+#pragma unroll
+              for (int q = 0; q < V; ++q) acc[u][q] = fmaf(g, f[q], acc[u][q]);
+            }
           }
         }
       }
@@ -136,10 +175,18 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   blocks = blocks / wpt * wpt;  // 8 * blocks warps: a multiple of wpt
   if (blocks < wpt) blocks = wpt;
   const unsigned grid = static_cast<unsigned>(need < blocks ? need : blocks);
-  if (a.dtype == MOE_F32)
-    combine_kernel<float><<<grid, 256, 0, stream>>>(a, static_cast<int>(wpt));
-  else
-    combine_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a, static_cast<int>(wpt));
+  const int w = static_cast<int>(wpt);
+  if (a.dtype == MOE_F32) {
+    if (a.k >= 2)
+      combine_kernel<float, true><<<grid, 256, 0, stream>>>(a, w);
+    else
+      combine_kernel<float, false><<<grid, 256, 0, stream>>>(a, w);
+  } else {
+    if (a.k >= 2)
+      combine_kernel<__nv_bfloat16, true><<<grid, 256, 0, stream>>>(a, w);
+    else
+      combine_kernel<__nv_bfloat16, false><<<grid, 256, 0, stream>>>(a, w);
+  }
   return cudaGetLastError();
 }
 
