@@ -458,6 +458,10 @@ def summarize(w, m, args, world):
         burst = peaks["bf16_tflops"] / (2.0 if w.dtype == "f32" else 1.0)
         roof["sampled_sm_mhz"] = mhz
         roof["frac_of_burst_at_sampled_clock"] = round(gemm_tflops / (burst * mhz / max_mhz), 4)
+    if roof["bound"] == "tensor":
+        # context only: against the cuBLAS rate held for seconds under the cap
+        sust = peaks["bf16_tflops_sustained"] / (2.0 if w.dtype == "f32" else 1.0)
+        roof["frac_of_sustained"] = round(gemm_tflops / sust, 4)
     sb = stage_bytes(w)
     stages = {}
     for name in ("route", "dispatch", "grouped_gemm", "combine"):
