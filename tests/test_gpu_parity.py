@@ -68,6 +68,9 @@ SMALL = {
     "pair_one_kstep": Workload("pair_one_kstep", T=1200, d=136, N=2, F=200, k=1, F_sh=72,
                                score="sigmoid", bias_zipf_s=1.1, bias_beta=0.3),
     "one_cta_odd_widths": Workload("one_cta_odd_widths", T=300, d=136, N=8, F=200, k=2),
+    # CTA pairs with output rows narrower than one 64-column store block
+    # (F = 48 act columns, d = 80 output columns: partial 128-byte segments)
+    "pair_narrow": Workload("pair_narrow", T=1100, d=80, N=2, F=48, k=2, F_sh=32),
     # >= 256 rows per expert on average: the grouped GEMM runs on CTA pairs
     # (256-row tiles)
     "pair_ragged": Workload("pair_ragged", T=1700, d=256, N=2, F=384, k=1),
