@@ -660,6 +660,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
   const int total = tile_start[G];
+  // Equal shares: the fewest CTAs that finish in the same number of rounds
+  // take all the tiles (CTA c: tiles c, c + stride, ...), so that a pass
+  // bound by reading its weights ends without a last round on a few SMs
+  // (896 tiles: 128 CTAs x 7 instead of 148 x 6 plus 8).
+  const int rounds = (total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  const int stride = rounds > 0 ? (total + rounds - 1) / rounds : static_cast<int>(gridDim.x);
+  const int first = static_cast<int>(blockIdx.x) < stride ? static_cast<int>(blockIdx.x) : total;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -669,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0, issued_mask = 0, issued_par = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = first; tile < total && ok; tile += stride) {
       int split = 0, kb0 = 0;
       TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
                                     : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
@@ -746,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = first; tile < total && ok; tile += stride) {
         int split = 0, kb0 = 0;
         TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
                                       : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
@@ -816,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_in_tile = quad * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = first; tile < total; tile += stride) {
       int split = 0, kb0 = 0;
       TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
                                     : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
