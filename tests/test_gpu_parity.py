@@ -349,13 +349,16 @@ def test_zero_weight_routed_experts_leave_shared_only(cuda_lib):
     assert_close_tol(np_f(r["out"]), ref, BF16_TOL, "shared only")
 
 
+@pytest.mark.parametrize("T", [300, 400])
 @pytest.mark.parametrize("score", ["softmax", "sigmoid"])
 @pytest.mark.parametrize("N,k", [(16, 4), (128, 1), (256, 8), (40, 16)])
-def test_route_tensor_core_exact_ties(cuda_lib, score, N, k):
+def test_route_tensor_core_exact_ties(cuda_lib, score, N, k, T):
     """bf16 routing from h runs as a tcgen05 GEMM with a top-k epilogue.
     Duplicated router rows give bitwise-equal logits; the lower expert index
-    must come first, exactly as the oracle orders equal scores."""
-    T, d = 300, 256
+    must come first, exactly as the oracle orders equal scores. Up to 128
+    experts a tile is 256 tokens in two 128-row halves: T = 300 leaves the
+    last tile's second half empty, T = 400 partly filled."""
+    d = 256
     gen = torch.Generator().manual_seed(N + k)
     h = torch.randn((T, d), generator=gen).to(torch.bfloat16)
     W = (torch.randn((N, d), generator=gen) * 0.05).to(torch.bfloat16)

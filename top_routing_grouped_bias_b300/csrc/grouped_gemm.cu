@@ -139,6 +139,9 @@ struct GemmParams {
   // a 1-row box and dispatched row r is h[gather_rows[r]] (TMA gather4).
   // Null: A0 is the dispatched copy x_disp.
   const int32_t* gather_rows;
+  // kRoute: 128-row halves per token tile (1, or 2 when N <= 128: 256 tokens
+  // per tile share each K-step's W_r operand)
+  int32_t row_halves;
 };
 
 struct TileInfo {
@@ -203,6 +206,22 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int* tile_start,
   const int bs = min(band_sz, mt - band * band_sz);
   ti.n_blk = r / bs;
   ti.m_blk = band * band_sz + (r - ti.n_blk * bs);
+  return ti;
+}
+
+// kRoute work unit: token tile `tile` of the single routed operand.
+__device__ __forceinline__ TileInfo route_tile(int tile, const GemmParams& p) {
+  TileInfo ti;
+  ti.g = 0;
+  ti.m_blk = tile;
+  ti.n_blk = 0;
+  ti.row0 = 0;
+  ti.rows = p.rows_routed;
+  ti.ncols = p.n_out;
+  ti.b_row0 = 0;
+  ti.num_kb = (p.K + 63) / 64;
+  ti.nr = 0;
+  ti.rv = 0;
   return ti;
 }
 
@@ -578,7 +597,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kRouter = MODE == kRoute || MODE == kLogits;
   const int mma_n = kRouter ? p.n_out : 256;
   const uint32_t idesc = make_idesc(kBM, mma_n, sizeof(T) == 2 ? 1u : 2u);
-  const uint32_t stage_tx = kRouter ? kStageA + static_cast<uint32_t>(mma_n) * 128u : kStageBytes;
+  // kRoute with two halves: a tile is 256 tokens, A0 in the A region, A1 and
+  // W_r in the B region; one W_r load per K-step serves both, accumulated
+  // into columns [0, n) and [128, 128 + n)
+  const int halves = MODE == kRoute ? p.row_halves : 1;
+  const uint32_t stage_tx = kRouter ? kStageA * static_cast<uint32_t>(halves) +
+                                          static_cast<uint32_t>(mma_n) * 128u
+                                    : kStageBytes;
 
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -642,7 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (g < G) {
         const int rows = g < p.n_routed ? grp_off[g + 1] - grp_off[g] : p.rows_shared;
         const int ncols = g < p.n_routed ? p.n_out : p.n_out_shared;
-        tiles = ((rows + kBM - 1) / kBM) * (MODE == kLogits ? p.k_splits : (ncols + BN - 1) / BN);
+        tiles = ((rows + kBM * halves - 1) / (kBM * halves)) *
+                (MODE == kLogits ? p.k_splits : (ncols + BN - 1) / BN);
       }
       int incl = tiles;
 #pragma unroll
@@ -678,8 +704,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = first; tile < total && ok; tile += stride) {
       int split = 0, kb0 = 0;
-      TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
-                                    : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+      TileInfo ti = MODE == kLogits  ? logits_tile(tile, p, split, kb0)
+                    : MODE == kRoute ? route_tile(tile, p)
+                                     : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
       set_swap<MODE, T>(ti, p);
       const bool dense = ti.g >= p.n_routed;
       const bool gather = MODE == kSwiGLU && p.gather_rows != nullptr && !dense;
@@ -689,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const void* mA = dense ? static_cast<const void*>(&mapA1) : static_cast<const void*>(&mapA0);
       const void* mB = dense ? static_cast<const void*>(&mapB1) : static_cast<const void*>(&mapB0);
       const void* mBu = dense ? static_cast<const void*>(&mapB1u) : static_cast<const void*>(&mapB0u);
-      const int a_row = ti.row0 + ti.m_blk * kBM;
+      const int a_row = ti.row0 + ti.m_blk * kBM * halves;
       const int b_row = ti.b_row0 + ti.n_blk * BN;
       int g4[4] = {0, 0, 0, 0};
       if (gather) {
@@ -731,6 +758,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (MODE == kSwiGLU) {
             tma_load_2d(sB, mB, &full_bar[stage], (kb0 + kb) * BK, b_row);
             tma_load_2d(sB + kStageB / 2, mBu, &full_bar[stage], (kb0 + kb) * BK, b_row);
+          } else if (MODE == kRoute && halves == 2) {
+            tma_load_2d(sB, mA, &full_bar[stage], (kb0 + kb) * BK, a_row + kBM);
+            tma_load_2d(sB + kStageA, mB, &full_bar[stage], (kb0 + kb) * BK, b_row);
           } else {
             tma_load_2d(sB, mB, &full_bar[stage], (kb0 + kb) * BK, b_row);
           }
@@ -755,8 +785,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = first; tile < total && ok; tile += stride) {
         int split = 0, kb0 = 0;
-        TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
-                                      : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+        TileInfo ti = MODE == kLogits  ? logits_tile(tile, p, split, kb0)
+                      : MODE == kRoute ? route_tile(tile, p)
+                                       : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
         set_swap<MODE, T>(ti, p);
         const uint32_t idesc_swap = make_idesc(kBM, ti.nr > 0 ? ti.nr : 16, 1u);
         if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, abort_v, p.status, p.budget_ns,
@@ -788,15 +819,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_f16(d_tmem + kAccCols / 2, w1, xd, idesc_swap, accum);
             }
           } else {
+            const bool two = MODE == kRoute && halves == 2;
+            const uint32_t w_addr = two ? b_addr + kStageA : b_addr;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t ad = sw128_kmajor_desc(a_addr + kk * 32);
-              const uint64_t bd = sw128_kmajor_desc(b_addr + kk * 32);
+              const uint64_t bd = sw128_kmajor_desc(w_addr + kk * 32);
               const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
               if (sizeof(T) == 2)
                 mma_f16(d_tmem, ad, bd, idesc, accum);
               else
                 mma_tf32(d_tmem, ad, bd, idesc, accum);
+              if (two)
+                mma_f16(d_tmem + kAccCols / 2, sw128_kmajor_desc(b_addr + kk * 32), bd, idesc,
+                        accum);
             }
           }
           mma_commit(&empty_bar[stage]);
@@ -825,10 +861,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = first; tile < total; tile += stride) {
       int split = 0, kb0 = 0;
-      TileInfo ti = MODE == kLogits ? logits_tile(tile, p, split, kb0)
-                                    : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
+      TileInfo ti = MODE == kLogits  ? logits_tile(tile, p, split, kb0)
+                    : MODE == kRoute ? route_tile(tile, p)
+                                     : decode_tile<BN, BK>(tile, tile_start, grp_off, G, p);
       set_swap<MODE, T>(ti, p);
-      const int row = ti.m_blk * kBM + row_in_tile;
+      const int row = ti.m_blk * kBM * halves + row_in_tile;
       const bool row_ok = row < ti.rows;
       const int col0 = ti.n_blk * BN;
       const int cols_left = ti.ncols - col0;
@@ -855,7 +892,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of the weight tile), its TMEM columns are the tile's rows
         swap_epilogue<MODE>(tbase, ti, row_in_tile, p);
       } else if (MODE == kRoute) {
-        route_epilogue<KT>(tbase, row, row_ok, p.n_out, p.re);
+#pragma unroll 1
+        for (int h = 0; h < halves; ++h)  // the tile's 128-row halves
+          route_epilogue<KT>(tbase + h * (kAccCols / 2), row + h * kBM, row + h * kBM < ti.rows,
+                             p.n_out, p.re);
       } else if (MODE == kLogits) {
         // this unit's partial logits, rows of the tile x n_out columns
         float* dst = p.partials +
@@ -1794,7 +1834,9 @@ cudaError_t launch_route_mma(const RouteArgs& a, cudaStream_t stream) {
   p.re.k = a.k;
   p.re.score = a.score;
   p.re.norm = a.norm;
-  int grid = static_cast<int>((a.T + kBM - 1) / kBM);
+  // up to 128 experts: 256-token tiles, two halves sharing each W_r load
+  p.row_halves = n_pad <= 128 ? 2 : 1;
+  int grid = static_cast<int>((a.T + kBM * p.row_halves - 1) / (kBM * p.row_halves));
   if (grid > num_sms()) grid = num_sms();
   using bf = __nv_bfloat16;
   if (a.k <= 1) return launch_gemm<kRoute, bf, 1>(m, p, grid, stream);
