@@ -18,6 +18,10 @@
 //   warps 2..5  epilogue: tcgen05.ld from TMEM, SiLU⊙up or plain convert,
 //               16-byte stores; double-buffered accumulators let the epilogue
 //               of one tile overlap the MMAs of the next
+// The CTAs share the tiles round-robin, over the fewest CTAs that finish in
+// the same number of rounds (a weight-bound pass then has no last round on a
+// few SMs). The CTA-pair kernel further down covers batches with many rows
+// per expert (256-row tiles, 128-byte row-segment stores).
 // For pass A the B tile stacks 128 rows of W_gate over the same 128 rows of
 // W_up, so one N=256 MMA produces the gate half (columns 0..127) and the up
 // half (128..255) of a 128-column output tile.
@@ -34,11 +38,13 @@
 //
 // Two more instances are the router: logits = h W_r^T for 128 tokens per tile
 // with all N <= 256 experts in one accumulator.
-//   kRoute   (batches of at least ~148 token tiles) does the whole routing in
+//   kRoute   (a split plan of one reduction slice: at least 75 token tiles,
+//            or d <= 448) does the whole routing in
 //            its epilogue: each thread takes one token's logit row from TMEM
 //            and computes softmax / sigmoid, the selection bias, the top-k
 //            with the lowest-index tie-break and the gates, overlapped with
-//            the next tile's MMAs.
+//            the next tile's MMAs. Up to 128 experts a tile is 256 tokens, two
+//            128-row halves that share each K-step's W_r load.
 //   kLogits  (smaller batches) splits the reduction over d into slices (one
 //            work unit per tile and slice) so that enough SMs stream h; each
 //            unit writes its fp32 partial logits and the warp-per-token
