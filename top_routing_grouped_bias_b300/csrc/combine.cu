@@ -53,11 +53,13 @@ constexpr int kCombineU = 4;
 // row's chunks of 32 * U vectors p, p + wpt, ...; each output vector still
 // comes from one lane with the same slot-order arithmetic.
 // kPair: two slots per step (k >= 2); top-1 keeps one, which needs fewer
-// registers and so more warps per SM.
-template <typename T, bool kPair>
+// registers and so more warps per SM. U: vectors per slot and lane per step
+// (two slots of U = 2 keep the registers low enough for four blocks per SM
+// when every warp has a token of its own; small batches, with several warps
+// per token, take U = 4).
+template <typename T, bool kPair, int U>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a, int wpt) {
   constexpr int V = 16 / sizeof(T);
-  constexpr int U = kCombineU;
   const int nvec = a.d / V;
   const uint4* Y = static_cast<const uint4*>(a.y_rows);
   const uint4* S = static_cast<const uint4*>(a.y_shared);
@@ -177,15 +179,19 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(need < blocks ? need : blocks);
   const int w = static_cast<int>(wpt);
   if (a.dtype == MOE_F32) {
-    if (a.k >= 2)
-      combine_kernel<float, true><<<grid, 256, 0, stream>>>(a, w);
+    if (a.k >= 2 && w == 1)
+      combine_kernel<float, true, 2><<<grid, 256, 0, stream>>>(a, w);
+    else if (a.k >= 2)
+      combine_kernel<float, true, 4><<<grid, 256, 0, stream>>>(a, w);
     else
-      combine_kernel<float, false><<<grid, 256, 0, stream>>>(a, w);
+      combine_kernel<float, false, kCombineU><<<grid, 256, 0, stream>>>(a, w);
   } else {
-    if (a.k >= 2)
-      combine_kernel<__nv_bfloat16, true><<<grid, 256, 0, stream>>>(a, w);
+    if (a.k >= 2 && w == 1)
+      combine_kernel<__nv_bfloat16, true, 2><<<grid, 256, 0, stream>>>(a, w);
+    else if (a.k >= 2)
+      combine_kernel<__nv_bfloat16, true, 4><<<grid, 256, 0, stream>>>(a, w);
     else
-      combine_kernel<__nv_bfloat16, false><<<grid, 256, 0, stream>>>(a, w);
+      combine_kernel<__nv_bfloat16, false, kCombineU><<<grid, 256, 0, stream>>>(a, w);
   }
   return cudaGetLastError();
 }
