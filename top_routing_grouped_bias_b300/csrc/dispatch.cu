@@ -8,14 +8,14 @@
 // on the ordering:
 //   1. count    per block of 256 tokens, per-expert pair counts -> base[e][b]
 //               (expert-major, so that each expert's column is contiguous)
-//   2. scan     counts[e] = sum_b (capped at the capacity when one is set),
-//               offsets = exclusive scan over e, base[e][b] = sum_{b' < b} count[b'][e]
-//               (one warp per expert column, 32 blocks per warp-scan step)
+//   2. scan     a block per expert column: base[e][b] = sum_{b' < b} count[b'][e],
+//               counts[e] = sum_b (capped at the capacity when one is set)
 //   3. permute  per block: for each warp and expert the mask of lanes holding
 //               it, scan of the masks' counts over warps (plus the block's
 //               base); rank = base + warp prefix + lower lanes holding e;
-//               row = offsets[e] + rank, or inv = -1 when rank >= capacity.
-//               Writes row_token and inv.
+//               row = offsets[e] + rank, or inv = -1 when rank >= capacity,
+//               with offsets = exclusive scan of counts over e (every block;
+//               block 0 writes them). Writes row_token and inv.
 //   4. gather   a warp per token at a time, up to eight 16-byte vectors of
 //               the row per lane in flight (batches of 8192 tokens or more;
 //               smaller ones a block per token, a thread per vector): reads
@@ -58,85 +58,81 @@ __global__ void __launch_bounds__(kTB) dispatch_count_kernel(DispatchArgs a) {
     a.block_base[static_cast<size_t>(e) * gridDim.x + blockIdx.x] = hist[e];
 }
 
-// One block of 1024 threads.
-__global__ void __launch_bounds__(1024) dispatch_scan_kernel(DispatchArgs a, int nb) {
-  __shared__ int tot[kMaxExperts];
-  __shared__ int warp_sums[32];
-  const int N = a.N;
-  // per-expert exclusive running sum over blocks: a warp takes one expert's
-  // column, 32 blocks per step (warp scan), four steps' loads in flight
-  {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    for (int e = w; e < N; e += nw) {
-      int carry = 0;
-      for (int b0 = 0; b0 < nb; b0 += 128) {
-        int c[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int b = b0 + 32 * u + lane;
-          c[u] = b < nb ? a.block_base[static_cast<size_t>(e) * nb + b] : 0;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int b = b0 + 32 * u + lane;
-          int incl = c[u];
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-          }
-          if (b < nb) a.block_base[static_cast<size_t>(e) * nb + b] = carry + incl - c[u];
-          carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-      }
-      // rows kept for this expert: all of them, or its first `capacity` pairs
-      if (lane == 0) tot[e] = a.cap_enabled && carry > a.capacity ? static_cast<int>(a.capacity) : carry;
-    }
-  }
-  __syncthreads();
-  // exclusive scan of tot[0..N) with one block: each thread owns a contiguous chunk
-  const int per = (N + blockDim.x - 1) / blockDim.x;
-  const int lo = threadIdx.x * per, hi = min(N, lo + per);
-  int local = 0;
-  for (int e = lo; e < hi; ++e) local += tot[e];
-  // block exclusive scan of `local`
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_sums[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    int v = lane < (blockDim.x >> 5) ? warp_sums[lane] : 0;
-    int inc = v;
+// One block per expert column: the exclusive running sum of the expert's
+// pair counts over the token blocks (base[e][b] = pairs of e in blocks
+// before b), and its total, capped at the capacity when one is set, written
+// to counts[e]. The offsets (a scan over the N totals) are left to the
+// permute kernel, whose every block needs them.
+__global__ void __launch_bounds__(kTB) dispatch_scan_kernel(DispatchArgs a, int nb) {
+  __shared__ int warp_sums[kWarps];
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int* col = a.block_base + static_cast<size_t>(e) * nb;
+  int carry = 0;
+  for (int b0 = 0; b0 < nb; b0 += kTB) {
+    const int b = b0 + static_cast<int>(threadIdx.x);
+    const int c = b < nb ? col[b] : 0;
+    int incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += u;
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
     }
-    warp_sums[lane] = inc - v;  // exclusive prefix of warps
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int ws = warp_sums[w];
+      before += w < warp ? ws : 0;
+      all += ws;
+    }
+    if (b < nb) col[b] = carry + before + incl - c;
+    carry += all;
+    __syncthreads();  // warp_sums is rewritten by the next step
   }
-  __syncthreads();
-  int run = warp_sums[w] + incl - local;
-  for (int e = lo; e < hi; ++e) {
-    a.counts[e] = tot[e];
-    a.offsets[e] = run;
-    run += tot[e];
-  }
-  if (hi == N && lo < hi) a.offsets[N] = run;  // the owner of expert N-1 (N >= 1)
+  // rows kept for this expert: all of them, or its first `capacity` pairs
+  if (threadIdx.x == 0)
+    a.counts[e] = a.cap_enabled && carry > a.capacity ? static_cast<int>(a.capacity) : carry;
 }
 
 __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
   extern __shared__ int sm[];
+  __shared__ int warp_sums[kWarps];
   const int N = a.N, k = a.k;
   unsigned* lanes = reinterpret_cast<unsigned*>(sm);   // [kWarps][N]: lanes holding e
   int* wbase = sm + kWarps * N;                        // [kWarps][N]: rank base of the warp
   int* sidx = sm + 2 * kWarps * N;                     // [kWarps][32][k]
+  int* off = sidx + kWarps * 32 * k;                   // [N + 1]: first row of each expert
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kWarps * N; i += blockDim.x) lanes[i] = 0u;
+  // offsets: exclusive scan of the capped totals over the experts, each
+  // thread a contiguous chunk of them (every block; block 0 writes them out)
+  {
+    const int per = (N + kTB - 1) / kTB;
+    const int lo = static_cast<int>(threadIdx.x) * per, hi = min(N, lo + per);
+    int local = 0;
+    for (int e = lo; e < hi; ++e) local += a.counts[e];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += warp_sums[w];
+    for (int e = lo; e < hi; ++e) {
+      off[e] = run;
+      if (blockIdx.x == 0) a.offsets[e] = run;
+      run += a.counts[e];
+    }
+    if (hi == N && lo < hi) {
+      off[N] = run;
+      if (blockIdx.x == 0) a.offsets[N] = run;
+    }
+  }
   __syncthreads();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kTB + threadIdx.x;
   const bool valid = t < a.T;
@@ -181,7 +177,7 @@ __global__ void __launch_bounds__(kTB) dispatch_permute_kernel(DispatchArgs a) {
         a.inv[t * k + j] = -1;  // beyond the expert's capacity: dropped
         continue;
       }
-      const int row = a.offsets[e] + rank;
+      const int row = off[e] + rank;
       a.row_token[row] = static_cast<int32_t>(t);
       a.inv[t * k + j] = row;
     }
@@ -437,8 +433,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
   } else {
     const int nb = static_cast<int>((a.T + kTB - 1) / kTB);
     dispatch_count_kernel<<<nb, kTB, a.N * sizeof(int), stream>>>(a);
-    dispatch_scan_kernel<<<1, 1024, 0, stream>>>(a, nb);
-    const size_t smem = sizeof(int) * (2 * static_cast<size_t>(kWarps) * a.N + kWarps * 32 * a.k);
+    dispatch_scan_kernel<<<a.N, kTB, 0, stream>>>(a, nb);
+    const size_t smem = sizeof(int) * (2 * static_cast<size_t>(kWarps) * a.N + kWarps * 32 * a.k +
+                                       static_cast<size_t>(a.N) + 1);
     cudaError_t err = cudaFuncSetAttribute(dispatch_permute_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
