@@ -224,7 +224,9 @@ def test_capacity_page1_table(cuda_lib):
 
 
 @pytest.mark.parametrize("T,N,k,C", [(3000, 8, 2, 0), (3000, 8, 2, 700), (3000, 8, 2, 10 ** 6),
-                                     (1000, 128, 8, 50), (513, 64, 1, 6)])
+                                     (1000, 128, 8, 50), (513, 64, 1, 6),
+                                     # the multi-block scan and the warp-per-token gather
+                                     (9000, 16, 3, 1200), (20000, 64, 2, 500)])
 def test_capacity_dispatch_random_exact(cuda_lib, T, N, k, C):
     gen = torch.Generator().manual_seed(T + C)
     # skewed routing so that some experts overflow

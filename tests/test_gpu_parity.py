@@ -324,6 +324,38 @@ def test_combine_page2_example(cuda_lib, dtype):
     assert (got[:, 2:] == 0).all()
 
 
+@pytest.mark.parametrize("dtype,T,d,k,shared", [
+    ("f32", 16, 1024, 2, False),    # two slots per step, four vectors, two warps per token
+    ("f32", 300, 256, 3, True),     # two vectors per slot, an odd slot count, shared rows
+    ("f32", 100, 36, 2, False),     # nine vectors per row
+    ("bf16", 8, 2048, 4, True),     # several warps per token, four vectors per slot
+    ("bf16", 1500, 264, 5, True),   # 33 vectors per row, an odd slot count
+    ("bf16", 2000, 512, 1, False),  # top-1: one slot per step
+])
+def test_combine_forms_vs_oracle(cuda_lib, dtype, T, d, k, shared):
+    """Every form of the combine kernel against the oracle's combine, within
+    one rounding of the fp32 slot-order sum; about 5 % of the slots are
+    dropped (inv = -1) and contribute nothing."""
+    gen = torch.Generator().manual_seed(T * 7 + d + k)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    R = T * k
+    y = torch.randn((R, d), generator=gen).to(tdt)
+    inv = torch.randperm(R, generator=gen).to(torch.int32).view(T, k).clone()
+    drop = torch.rand((T, k), generator=gen) < 0.05
+    inv[drop] = -1
+    gate = torch.rand((T, k), generator=gen)
+    ysh = torch.randn((T, d), generator=gen).to(tdt) if shared else None
+    cfg = api.make_config(T, d, 16, k, 64, dtype=dtype)
+    out = torch.empty((T, d), dtype=tdt, device="cuda")
+    api.moe_combine(cfg, y.cuda(), inv.cuda(), gate.cuda(), None if ysh is None else ysh.cuda(),
+                    out)
+    torch.cuda.synchronize()
+    # a dropped slot is the same as a zero gate on any row
+    r = {"y_rows": y, "inv": torch.where(drop, torch.zeros_like(inv), inv),
+         "gate": torch.where(drop, torch.zeros_like(gate), gate), "y_sh": ysh, "out": out}
+    check_combine(r, cfg, f"combine {dtype} T={T} d={d} k={k}")
+
+
 # ------------------------------------------------------------ expert FFN ---
 def test_single_expert_is_dense_swiglu_vs_library(cuda_lib):
     """N=1, k=1: the grouped GEMM pair is a plain SwiGLU FFN; check against
