@@ -39,3 +39,42 @@ def test_launches_per_forward_follow_the_router_plan():
     assert bench.kernels_per_forward(W["switch_top1"]) == 7         # fused router, fused combine
     assert bench.kernels_per_forward(W["tiny_fp32"]) == 6           # CUDA-core router, one-block dispatch
     assert bench.kernels_per_forward(W["fine_grained_shared"]) == 9  # split router, four-launch dispatch
+
+
+def _measurement(w, gemm_ms, region_s, mhz):
+    import numpy as np
+    counts = np.full(w.N, w.T * w.k // w.N)
+    return {"counts": counts, "ms": gemm_ms * 1.05, "e2e_ms": gemm_ms * 1.1,
+            "staged_ms": gemm_ms * 1.06, "region_s": region_s,
+            "stage_ms": {"route": 0.02, "dispatch": 0.03, "grouped_gemm": gemm_ms, "combine": 0.02},
+            "clocks": {"sm_mhz": mhz, "sm_max_mhz": 2032.0, "reasons": []}}
+
+
+def test_roofline_arithmetic_of_the_bench_line():
+    """The grouped GEMM's fraction against the burst peak for a short region,
+    against the sustained one for a region over 0.5 s, plus the two context
+    fractions; a weight-bound batch is held against HBM, with the whole
+    layer's fraction beside it."""
+    import argparse
+    args = argparse.Namespace(steps=10)
+    peaks, _ = bench.load_peaks()
+    w = synth.WORKLOADS["mixtral_prefill"]
+    flops = bench.workload_work(w)["gemm_flops"]
+    out = bench.summarize(w, _measurement(w, 2.0, 0.1, 1016.0), args, 1)
+    r = out["roofline"]
+    achieved = flops / 2.0e-3 / 1e12
+    assert r["bound"] == "tensor" and abs(r["achieved"] - achieved) < 0.01
+    assert abs(r["frac"] - achieved / peaks["bf16_tflops"]) < 1e-4
+    assert abs(r["frac_of_sustained"] - achieved / peaks["bf16_tflops_sustained"]) < 1e-4
+    # half the maximum clock: the burst peak scaled by 0.5
+    assert abs(r["frac_of_burst_at_sampled_clock"] - 2 * r["frac"]) < 1e-3
+    long = bench.summarize(w, _measurement(w, 2.0, 1.0, 1016.0), args, 1)["roofline"]
+    assert abs(long["frac"] - achieved / peaks["bf16_tflops_sustained"]) < 1e-4
+    assert out["tokens_per_s"] == round(w.T * 10 / (2.1 * 10 / 1e3), 1)
+    # decode: about 4 rows per expert, weight-bandwidth bound
+    wd = synth.WORKLOADS["mixtral_decode"]
+    dec = bench.summarize(wd, _measurement(wd, 0.45, 0.03, 2032.0), args, 1)
+    gb = bench.gemm_bytes(wd, _measurement(wd, 0.45, 0.03, 2032.0)["counts"])
+    assert dec["roofline"]["bound"] == "hbm"
+    assert abs(dec["roofline"]["frac"] - gb / 0.45e-3 / 1e9 / peaks["hbm_gbs"]) < 1e-4
+    assert "layer_hbm" in dec and dec["layer_hbm"]["frac"] < dec["roofline"]["frac"]
